@@ -1,0 +1,282 @@
+/*
+ * Plain CPU oracle for the forward pass of Beam's Mixture-of-Experts block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg do.  It shares no code, header, table or
+ * constant with the CUDA library.
+ *
+ * What it computes (sources are the five web pages about Reflection's Beam):
+ *   - "Hugging Face releases Beam ..." (deliver-ai.xyz), third paragraph:
+ *     256 experts per layer, each a SwiGLU MLP with intermediate size 2,560;
+ *     the router keeps the top 4 of 8 groups (32 experts each) and selects
+ *     the top 8 experts inside them.
+ *   - "Reflection Releases Beam ..." (telohudelo.online), section "Where Beam
+ *     Saves and Where the Memory Bill Comes In": sigmoid scores, DeepSeek-V3
+ *     style group limits, no shared expert, normalised and scaled by 2.5.
+ *   - "Beam 1.0" (interestana.com digest): auxiliary-loss-free balancing with
+ *     a per-expert bias.
+ * The pages leave several steps open; the readings taken here are:
+ *   - group score = sum of the two largest biased scores in the group;
+ *   - experts are selected on biased scores s+b, weighted by unbiased s;
+ *   - the 8 weights are normalised to sum to 1, then multiplied by 2.5;
+ *   - experts outside the kept groups are excluded (never selected), not
+ *     given a score of 0;
+ *   - ties go to the lower group index, then to the lower expert index; the
+ *     output order of the k experts is descending biased score.
+ *
+ * Precision: every decision value (logit, sigmoid score, biased score, group
+ * score) is held in fp32, the precision the GPU path decides in; each is
+ * computed in fp64 and rounded once to fp32, except s+b and top1+top2 which
+ * are single fp32 additions.  The expert path (SwiGLU MLP and the weighted
+ * sum) runs entirely in fp64.
+ *
+ * Parity pins for every function are in tests/test_oracle_*.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+
+/* ---- scalar decoders (from the formats' definitions) ------------------- */
+
+/* bf16 is the upper half of an IEEE binary32. */
+static double bf16_value(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* FP4 E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; no inf/nan. */
+double oracle_e2m1_value(uint8_t code) {
+  int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+/* FP8 E4M3 (the "fn" flavour): 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+ * exponent 15 with mantissa 7 is NaN, there is no infinity. */
+double oracle_e4m3_value(uint8_t code) {
+  int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) mag = ldexp(m / 8.0, -6);
+  else mag = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* ---- routing ----------------------------------------------------------- */
+
+/*
+ * Router of one MoE block, for T tokens.
+ *   x         bf16 [T, H]   token activations (row-major)
+ *   w_router  fp32 [E, H]   router weight, one row per expert
+ *   bias      fp32 [E]      per-expert selection bias
+ *   topk_idx  int32 [T, k]  selected experts, descending biased score
+ *   topk_w    fp32 [T, k]   routed weights (sum to routed_scale)
+ * Optional outputs (NULL to skip): logits/scores/biased [T, E] fp32,
+ * group_score [T, G] fp32, group_kept [T, G] uint8.
+ */
+int oracle_route(int T, int H, int E, int n_group, int topk_group, int top_k,
+                 float routed_scale, const uint16_t *x, const float *w_router,
+                 const float *bias, int32_t *topk_idx, float *topk_w,
+                 float *logits_out, float *scores_out, float *biased_out,
+                 float *group_score_out, uint8_t *group_kept_out) {
+  if (T < 0 || H <= 0 || E <= 0 || n_group <= 0 || E % n_group != 0) return ORACLE_BAD_ARG;
+  const int gsize = E / n_group;
+  if (gsize < 2 || topk_group <= 0 || topk_group > n_group) return ORACLE_BAD_ARG;
+  if (top_k <= 0 || top_k > topk_group * gsize) return ORACLE_BAD_ARG;
+
+  int bad = 0;
+#pragma omp parallel
+  {
+    float *logit = (float *)malloc(sizeof(float) * E);
+    float *s = (float *)malloc(sizeof(float) * E);
+    float *sb = (float *)malloc(sizeof(float) * E);
+    float *gs = (float *)malloc(sizeof(float) * n_group);
+    uint8_t *kept = (uint8_t *)malloc(n_group);
+    if (!logit || !s || !sb || !gs || !kept) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(static)
+      for (int t = 0; t < T; ++t) {
+        const uint16_t *xt = x + (size_t)t * H;
+        /* logits: fp64 products and sum, one rounding to fp32 */
+        for (int e = 0; e < E; ++e) {
+          const float *we = w_router + (size_t)e * H;
+          double acc = 0.0;
+          for (int h = 0; h < H; ++h) acc += bf16_value(xt[h]) * (double)we[h];
+          logit[e] = (float)acc;
+        }
+        /* sigmoid affinity, and the biased score used only for selection */
+        for (int e = 0; e < E; ++e) {
+          s[e] = (float)(1.0 / (1.0 + exp(-(double)logit[e])));
+          sb[e] = s[e] + bias[e];
+        }
+        /* group score: the two largest biased scores of the group, added */
+        for (int j = 0; j < n_group; ++j) {
+          float a1 = -INFINITY, a2 = -INFINITY;
+          for (int i = 0; i < gsize; ++i) {
+            float v = sb[j * gsize + i];
+            if (v > a1) { a2 = a1; a1 = v; }
+            else if (v > a2) { a2 = v; }
+          }
+          gs[j] = a1 + a2;
+        }
+        /* keep a group when fewer than topk_group groups beat it; a group
+         * beats another with a larger score, or an equal one and a lower index */
+        for (int j = 0; j < n_group; ++j) {
+          int rank = 0;
+          for (int j2 = 0; j2 < n_group; ++j2)
+            if (gs[j2] > gs[j] || (gs[j2] == gs[j] && j2 < j)) ++rank;
+          kept[j] = rank < topk_group;
+        }
+        /* expert rank among the candidates (experts of kept groups) */
+        int32_t *idx = topk_idx + (size_t)t * top_k;
+        for (int e = 0; e < E; ++e) {
+          if (!kept[e / gsize]) continue;
+          int rank = 0;
+          for (int e2 = 0; e2 < E; ++e2) {
+            if (!kept[e2 / gsize]) continue;
+            if (sb[e2] > sb[e] || (sb[e2] == sb[e] && e2 < e)) ++rank;
+          }
+          if (rank < top_k) idx[rank] = e;
+        }
+        /* weights from the unbiased scores, normalised, times routed_scale */
+        double sum = 0.0;
+        for (int k = 0; k < top_k; ++k) sum += (double)s[idx[k]];
+        for (int k = 0; k < top_k; ++k)
+          topk_w[(size_t)t * top_k + k] =
+              (float)((double)routed_scale * (double)s[idx[k]] / sum);
+
+        if (logits_out) memcpy(logits_out + (size_t)t * E, logit, sizeof(float) * E);
+        if (scores_out) memcpy(scores_out + (size_t)t * E, s, sizeof(float) * E);
+        if (biased_out) memcpy(biased_out + (size_t)t * E, sb, sizeof(float) * E);
+        if (group_score_out) memcpy(group_score_out + (size_t)t * n_group, gs, sizeof(float) * n_group);
+        if (group_kept_out) memcpy(group_kept_out + (size_t)t * n_group, kept, n_group);
+      }
+    }
+    free(logit); free(s); free(sb); free(gs); free(kept);
+  }
+  return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
+/* ---- expert weights ---------------------------------------------------- */
+
+/* One weight matrix [N, K] (out x in, K contiguous) of one expert.
+ * dtype 0: bf16, data is uint16 [N, K].
+ * dtype 1: NVFP4, data is uint8 [N, K/2] (low nibble = even k), scales is
+ *          e4m3 uint8 [N, K/16], and the value is e2m1 * e4m3 * global. */
+typedef struct {
+  int dtype;
+  const void *data;
+  const uint8_t *scales;
+  double global;
+} oracle_matrix;
+
+static void decode_row(const oracle_matrix *m, int K, int row, double *out) {
+  if (m->dtype == 0) {
+    const uint16_t *r = (const uint16_t *)m->data + (size_t)row * K;
+    for (int k = 0; k < K; ++k) out[k] = bf16_value(r[k]);
+  } else {
+    const uint8_t *q = (const uint8_t *)m->data + (size_t)row * (K / 2);
+    const uint8_t *sc = m->scales + (size_t)row * (K / 16);
+    for (int k = 0; k < K; ++k) {
+      uint8_t byte = q[k / 2];
+      uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+      out[k] = oracle_e2m1_value(code) * oracle_e4m3_value(sc[k / 16]) * m->global;
+    }
+  }
+}
+
+/* Dequantise (or widen) a whole matrix to fp64 [N, K]. */
+int oracle_decode_matrix(int dtype, int N, int K, const void *data,
+                         const uint8_t *scales, double global, double *out) {
+  if (N <= 0 || K <= 0 || (dtype == 1 && K % 16 != 0)) return ORACLE_BAD_ARG;
+  oracle_matrix m = {dtype, data, scales, global};
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) decode_row(&m, K, n, out + (size_t)n * K);
+  return ORACLE_OK;
+}
+
+/*
+ * One SwiGLU expert applied to n rows:
+ *   o[r] = W_down . ( silu(W_gate . x[r]) * (W_up . x[r]) ),   silu(z) = z / (1 + e^-z)
+ *   x      bf16 [n, H]
+ *   W_gate [I, H], W_up [I, H], W_down [H, I]  (bf16 or NVFP4, see oracle_matrix)
+ *   o      fp64 [n, H]
+ * All arithmetic in fp64.
+ */
+int oracle_expert_swiglu(int n, int H, int I, const uint16_t *x,
+                         int dtype, const void *wg, const uint8_t *sg, double gg,
+                         const void *wu, const uint8_t *su, double gu,
+                         const void *wd, const uint8_t *sd, double gd,
+                         double *o) {
+  if (n < 0 || H <= 0 || I <= 0) return ORACLE_BAD_ARG;
+  if (n == 0) return ORACLE_OK;
+  oracle_matrix mg = {dtype, wg, sg, gg}, mu = {dtype, wu, su, gu}, md = {dtype, wd, sd, gd};
+  double *xd = (double *)malloc(sizeof(double) * (size_t)n * H);
+  double *act = (double *)malloc(sizeof(double) * (size_t)n * I);
+  if (!xd || !act) { free(xd); free(act); return ORACLE_BAD_ARG; }
+  for (size_t i = 0; i < (size_t)n * H; ++i) xd[i] = bf16_value(x[i]);
+
+#pragma omp parallel
+  {
+    double *rg = (double *)malloc(sizeof(double) * H);
+    double *ru = (double *)malloc(sizeof(double) * H);
+#pragma omp for schedule(static)
+    for (int i = 0; i < I; ++i) {
+      decode_row(&mg, H, i, rg);
+      decode_row(&mu, H, i, ru);
+      for (int r = 0; r < n; ++r) {
+        const double *xr = xd + (size_t)r * H;
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) { g += rg[h] * xr[h]; u += ru[h] * xr[h]; }
+        act[(size_t)r * I + i] = g / (1.0 + exp(-g)) * u;
+      }
+    }
+    free(rg); free(ru);
+  }
+#pragma omp parallel
+  {
+    double *rd = (double *)malloc(sizeof(double) * I);
+#pragma omp for schedule(static)
+    for (int j = 0; j < H; ++j) {
+      decode_row(&md, I, j, rd);
+      for (int r = 0; r < n; ++r) {
+        const double *ar = act + (size_t)r * I;
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += rd[i] * ar[i];
+        o[(size_t)r * H + j] = acc;
+      }
+    }
+    free(rd);
+  }
+  free(xd); free(act);
+  return ORACLE_OK;
+}
+
+/*
+ * Weighted combine: y[t] = sum over k = 0..top_k-1, in that order, of
+ * topk_w[t,k] * o[t,k,:].  o is fp64 [T, top_k, H]; y is fp64 [T, H].
+ * There is no shared expert, so nothing else enters y.
+ */
+int oracle_combine(int T, int top_k, int H, const float *topk_w, const double *o, double *y) {
+  if (T < 0 || top_k <= 0 || H <= 0) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    double *yt = y + (size_t)t * H;
+    for (int h = 0; h < H; ++h) yt[h] = 0.0;
+    for (int k = 0; k < top_k; ++k) {
+      double w = (double)topk_w[(size_t)t * top_k + k];
+      const double *ok = o + ((size_t)t * top_k + k) * H;
+      for (int h = 0; h < H; ++h) yt[h] += w * ok[h];
+    }
+  }
+  return ORACLE_OK;
+}
