@@ -1,0 +1,245 @@
+"""Python binding of libbeam_moe.so, the sm_103a forward pass of Beam's
+Mixture-of-Experts block (sigmoid router with selection bias and
+group-limited top-k, dispatch, SwiGLU experts, combine).
+
+Argument marshalling only: every function here checks tensor dtypes, shapes
+and devices, then calls the C entry point of the same name in
+``include/beam_moe.h`` with raw device pointers and the current CUDA stream.
+Every step of the computation runs in the library's kernels; there is no
+fallback, and importing this package fails if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing; build it with `python -m group_limited_routing_bias_b300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+MOE_W_BF16, MOE_W_NVFP4 = 0, 1
+MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_EXPERTS, MOE_OP_FORWARD = 0, 1, 2, 3
+MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
+
+EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
+            "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
+            "moe_experts_swiglu", "moe_combine", "moe_forward")
+
+
+class MoeDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int),
+                ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("I", ctypes.c_int), ("routed_scale", ctypes.c_float)]
+
+
+class MoeExperts(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int),
+                ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p)]
+
+
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_DP = ctypes.POINTER(MoeDims)
+_sig = {
+    "moe_version": ([], _I),
+    "moe_status_string": ([_I], ctypes.c_char_p),
+    "moe_check_dims": ([_DP], _I),
+    "moe_workspace_size": ([_DP, _I, _I], _S),
+    "moe_workspace_init": ([_P, _P], _I),
+    "moe_workspace_status": ([_P, _P, ctypes.POINTER(ctypes.c_uint32)], _I),
+    "moe_route": ([_DP, _P, _P, _P, _P, _P, _P, _S, _P], _I),
+    "moe_permute": ([_DP, _P, _P, _P, _P, _P, _P, _P, _S, _P], _I),
+    "moe_experts_swiglu": ([_DP, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _P, _P, _S, _P], _I),
+    "moe_combine": ([_DP, _P, _P, _P, _P], _I),
+    "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
+}
+for _name, (_args, _ret) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _ret
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def status_string(status: int) -> str:
+    return _lib.moe_status_string(status).decode()
+
+
+def version() -> int:
+    return _lib.moe_version()
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def make_dims(T, H, E, n_group, topk_group, top_k, I, routed_scale) -> MoeDims:
+    return MoeDims(T, H, E, n_group, topk_group, top_k, I, routed_scale)
+
+
+def dims_of(cfg, T: Optional[int] = None) -> MoeDims:
+    """Dims from any object with the fields T, H, E, n_group, topk_group, top_k, I, routed_scale."""
+    return MoeDims(cfg.T if T is None else T, cfg.H, cfg.E, cfg.n_group, cfg.topk_group, cfg.top_k,
+                   cfg.I, cfg.routed_scale)
+
+
+def check_dims(d: MoeDims) -> int:
+    return _lib.moe_check_dims(ctypes.byref(d))
+
+
+def workspace_size(d: MoeDims, op: int, wdtype: int = MOE_W_BF16) -> int:
+    return _lib.moe_workspace_size(ctypes.byref(d), wdtype, op)
+
+
+def alloc_workspace(d: MoeDims, op: int, wdtype: int = MOE_W_BF16, device="cuda") -> torch.Tensor:
+    """A zeroed workspace of the right size (device memory from torch's allocator)."""
+    n = workspace_size(d, op, wdtype)
+    if n == 0:
+        raise MoeError("moe_workspace_size", 2)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, shape=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the workspace's device status bits."""
+    bits = ctypes.c_uint32(0)
+    st = _lib.moe_workspace_status(_ptr(ws, torch.uint8, name="ws"), _stream(stream), ctypes.byref(bits))
+    if st not in (MOE_OK, 5):
+        raise MoeError("moe_workspace_status", st)
+    return bits.value
+
+
+def workspace_init(ws: torch.Tensor, stream=None):
+    _check("moe_workspace_init", _lib.moe_workspace_init(_ptr(ws, torch.uint8, name="ws"), _stream(stream)))
+
+
+@dataclass
+class Experts:
+    """Expert weights of one layer.
+
+    bf16: w_gate, w_up [E, I, H], w_down [E, H, I].
+    NVFP4: w_* packed e2m1 uint8 [E, N, K/2], s_* e4m3 uint8 [E, N, K/16], g_* fp32 [E].
+    """
+    w_gate: torch.Tensor
+    w_up: torch.Tensor
+    w_down: torch.Tensor
+    s_gate: Optional[torch.Tensor] = None
+    s_up: Optional[torch.Tensor] = None
+    s_down: Optional[torch.Tensor] = None
+    g_gate: Optional[torch.Tensor] = None
+    g_up: Optional[torch.Tensor] = None
+    g_down: Optional[torch.Tensor] = None
+
+    @property
+    def dtype(self) -> int:
+        return MOE_W_NVFP4 if self.w_gate.dtype == torch.uint8 else MOE_W_BF16
+
+    def struct(self, d: MoeDims) -> MoeExperts:
+        E, H, I = d.E, d.H, d.I
+        if self.dtype == MOE_W_BF16:
+            bf = torch.bfloat16
+            return MoeExperts(MOE_W_BF16, _ptr(self.w_gate, bf, (E, I, H), "w_gate"),
+                              _ptr(self.w_up, bf, (E, I, H), "w_up"),
+                              _ptr(self.w_down, bf, (E, H, I), "w_down"), None, None, None, None,
+                              None, None)
+        u8, f32 = torch.uint8, torch.float32
+        return MoeExperts(MOE_W_NVFP4,
+                          _ptr(self.w_gate, u8, (E, I, H // 2), "w_gate"),
+                          _ptr(self.w_up, u8, (E, I, H // 2), "w_up"),
+                          _ptr(self.w_down, u8, (E, H, I // 2), "w_down"),
+                          _ptr(self.s_gate, u8, (E, I, H // 16), "s_gate"),
+                          _ptr(self.s_up, u8, (E, I, H // 16), "s_up"),
+                          _ptr(self.s_down, u8, (E, H, I // 16), "s_down"),
+                          _ptr(self.g_gate, f32, (E,), "g_gate"), _ptr(self.g_up, f32, (E,), "g_up"),
+                          _ptr(self.g_down, f32, (E,), "g_down"))
+
+
+def moe_route(d: MoeDims, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
+    """Router; fills topk_idx int32 [T,k] and topk_w fp32 [T,k]."""
+    T, H, E, k = d.T, d.H, d.E, d.top_k
+    _check("moe_route", _lib.moe_route(
+        ctypes.byref(d), _ptr(x, torch.bfloat16, (T, H), "x"),
+        _ptr(w_router, torch.float32, (E, H), "w_router"), _ptr(bias, torch.float32, (E,), "bias"),
+        _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
+
+
+def moe_permute(d: MoeDims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src, ws, stream=None):
+    """Dispatch; fills expert_offsets [E+1], slot_of [T*k], row_src [T*k], x_perm [T*k, H]."""
+    T, H, E, Tk = d.T, d.H, d.E, d.T * d.top_k
+    _check("moe_permute", _lib.moe_permute(
+        ctypes.byref(d), _ptr(topk_idx, torch.int32, (T, d.top_k), "topk_idx"),
+        _ptr(x, torch.bfloat16, (T, H), "x"), _ptr(x_perm, torch.bfloat16, (Tk, H), "x_perm"),
+        _ptr(expert_offsets, torch.int32, (E + 1,), "expert_offsets"),
+        _ptr(slot_of, torch.int32, (Tk,), "slot_of"), _ptr(row_src, torch.int32, (Tk,), "row_src"),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
+
+
+def moe_experts_swiglu(d: MoeDims, experts: Experts, x_perm, expert_offsets, row_src, topk_w,
+                       y_partial, ws, stream=None):
+    """Expert SwiGLU MLPs over permuted rows; fills y_partial bf16 [T*k, H]."""
+    Tk, H, E = d.T * d.top_k, d.H, d.E
+    ex = experts.struct(d)
+    _check("moe_experts_swiglu", _lib.moe_experts_swiglu(
+        ctypes.byref(d), ctypes.byref(ex), _ptr(x_perm, torch.bfloat16, (Tk, H), "x_perm"),
+        _ptr(expert_offsets, torch.int32, (E + 1,), "expert_offsets"),
+        _ptr(row_src, torch.int32, (Tk,), "row_src"),
+        _ptr(topk_w, torch.float32, (d.T, d.top_k), "topk_w"),
+        _ptr(y_partial, torch.bfloat16, (Tk, H), "y_partial"),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
+
+
+def moe_combine(d: MoeDims, y_partial, slot_of, y, stream=None):
+    """Deterministic combine; fills y bf16 [T, H]."""
+    Tk, H = d.T * d.top_k, d.H
+    _check("moe_combine", _lib.moe_combine(
+        ctypes.byref(d), _ptr(y_partial, torch.bfloat16, (Tk, H), "y_partial"),
+        _ptr(slot_of, torch.int32, (Tk,), "slot_of"), _ptr(y, torch.bfloat16, (d.T, H), "y"),
+        _stream(stream)))
+
+
+def moe_forward(d: MoeDims, x, w_router, bias, experts: Experts, y, ws, topk_idx=None, topk_w=None,
+                stream=None):
+    """The whole block; fills y bf16 [T, H] (and the routing, when given buffers)."""
+    T, H, E, k = d.T, d.H, d.E, d.top_k
+    ex = experts.struct(d)
+    _check("moe_forward", _lib.moe_forward(
+        ctypes.byref(d), _ptr(x, torch.bfloat16, (T, H), "x"),
+        _ptr(w_router, torch.float32, (E, H), "w_router"), _ptr(bias, torch.float32, (E,), "bias"),
+        ctypes.byref(ex), _ptr(y, torch.bfloat16, (T, H), "y"),
+        _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))

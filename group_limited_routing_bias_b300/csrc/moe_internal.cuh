@@ -1,0 +1,128 @@
+// Declarations shared by the translation units of libbeam_moe.so: launch
+// plans, the workspace layout, and tensor-map creation.
+#pragma once
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "beam_moe.h"
+
+namespace beam {
+
+constexpr int kTargetCtas = 148;       // B300 SM count; sizes the router's K split
+constexpr int kPermuteChunk = 4096;    // entries per permute CTA (32 warps x 128)
+constexpr size_t kHeaderBytes = 256;   // workspace status header
+
+inline int ilog2(int v) {
+  int r = 0;
+  while ((1 << (r + 1)) <= v) ++r;
+  return r;
+}
+
+// ------------------------------------------------------------------ plans
+
+struct RouterPlan {
+  int T, E, H;
+  int BN;      // MMA N: next of 32/64/128/256 at or above E
+  int ksplit;  // CTAs along K (partial sums added in order by the top-k kernel)
+};
+
+inline RouterPlan make_router_plan(const moe_dims &d) {
+  RouterPlan p;
+  p.T = d.T;
+  p.E = d.E;
+  p.H = d.H;
+  p.BN = d.E <= 32 ? 32 : d.E <= 64 ? 64 : d.E <= 128 ? 128 : 256;
+  const int mt = std::max(1, (d.T + 127) / 128);
+  const int ksteps = 3 * d.H / 64;
+  p.ksplit = std::max(1, std::min(kTargetCtas / mt, ksteps / 4));
+  return p;
+}
+
+// Expert GEMM plan: N of the MMA (token rows per tile) from the mean rows per expert.
+inline int expert_bn(const moe_dims &d) {
+  const long rows = (long)d.T * d.top_k;
+  const long mean = (rows + d.E - 1) / d.E;
+  return mean <= 16 ? 16 : mean <= 32 ? 32 : mean <= 64 ? 64 : mean <= 128 ? 128 : 256;
+}
+
+// ------------------------------------------------------------------ workspace
+
+struct WsLayout {
+  size_t w3 = 0, partial = 0;                       // router
+  size_t topk_idx = 0, topk_w = 0;                  // forward only
+  size_t counts = 0, bases = 0;                     // permute
+  size_t offsets = 0, slot_of = 0, row_src = 0, x_perm = 0;  // forward only
+  size_t h = 0;                                     // experts
+  size_t y_partial = 0;                             // forward only
+  size_t total = 0;
+};
+
+inline WsLayout ws_layout(const moe_dims &d, moe_op op) {
+  WsLayout L;
+  size_t off = kHeaderBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  const size_t Tk = (size_t)d.T * d.top_k;
+  const bool fwd = op == MOE_OP_FORWARD;
+  if (op == MOE_OP_ROUTE || fwd) {
+    const RouterPlan rp = make_router_plan(d);
+    L.w3 = take((size_t)d.E * 3 * d.H * 2);
+    L.partial = take((size_t)rp.ksplit * d.T * d.E * 4);
+  }
+  if (fwd) {
+    L.topk_idx = take(Tk * 4);
+    L.topk_w = take(Tk * 4);
+  }
+  if (op == MOE_OP_PERMUTE || fwd) {
+    const size_t nchunks = std::max<size_t>(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
+    L.counts = take(nchunks * d.E * 4);
+    L.bases = take(nchunks * d.E * 4);
+  }
+  if (fwd) {
+    L.offsets = take((size_t)(d.E + 1) * 4);
+    L.slot_of = take(Tk * 4);
+    L.row_src = take(Tk * 4);
+    L.x_perm = take(Tk * d.H * 2);
+  }
+  if (op == MOE_OP_EXPERTS || fwd) L.h = take(Tk * d.I * 2);
+  if (fwd) L.y_partial = take(Tk * d.H * 2);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+// 2-D bf16 tensor [outer, inner] (inner contiguous), box {64, box_outer},
+// 128-byte swizzle, zero fill out of bounds.
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                       uint32_t box_outer);
+
+int device_sm_count();
+
+// ------------------------------------------------------------------ launchers
+
+moe_status launch_route(const moe_dims &d, const void *x, const float *w_router, const float *bias,
+                        int32_t *topk_idx, float *topk_w, const RouterPlan &rp,
+                        __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream);
+
+moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
+                          int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
+                          int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream);
+
+moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *x_perm,
+                          const int32_t *expert_offsets, const int32_t *row_src,
+                          const float *topk_w, void *y_partial, __nv_bfloat16 *h,
+                          uint32_t *status, cudaStream_t stream);
+
+moe_status launch_combine(const moe_dims &d, const void *y_partial, const int32_t *slot_of, void *y,
+                          cudaStream_t stream);
+
+}  // namespace beam

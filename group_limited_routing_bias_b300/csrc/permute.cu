@@ -1,0 +1,179 @@
+// Dispatch of the Beam MoE block: the T*k (token, slot) entries are counted
+// per expert, offsets are the exclusive scan of the counts, and every entry
+// gets a row in expert-major order that keeps ascending entry order inside an
+// expert (a stable counting sort).  Then the x rows are gathered into that
+// order so each expert's rows are contiguous for the grouped GEMMs.
+//
+//   permute_count_kernel   one CTA per chunk of 4096 entries: histogram
+//   permute_scan_kernel    one CTA: per-chunk bases and expert offsets
+//   permute_scatter_kernel one CTA per chunk: warp-ordered ranks -> slots
+//   permute_gather_kernel  all SMs: copy x rows into x_perm (16-byte vectors)
+#include "moe_internal.cuh"
+
+namespace beam {
+
+namespace {
+
+constexpr int kChunkThreads = 1024;
+constexpr int kEntriesPerWarp = kPermuteChunk / (kChunkThreads / 32);  // 128
+
+__global__ void __launch_bounds__(kChunkThreads)
+    permute_count_kernel(const int32_t *__restrict__ idx, int Tk, int E, int32_t *__restrict__ counts,
+                         uint32_t *status) {
+  extern __shared__ int cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kPermuteChunk;
+  bool bad = false;
+  for (int j = threadIdx.x; j < kPermuteChunk; j += blockDim.x) {
+    const int n = base + j;
+    if (n >= Tk) break;
+    const int e = idx[n];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(status, (uint32_t)MOE_DEV_BAD_INDEX);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// Exclusive block scan of one value per thread (blockDim.x <= 1024).
+__device__ int block_exclusive_scan(int v, int *warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int s = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
+    }
+    if (lane < nw) warp_sums[lane] = s;  // inclusive sums of warps
+  }
+  __syncthreads();
+  const int before = warp == 0 ? 0 : warp_sums[warp - 1];
+  return before + incl - v;
+}
+
+__global__ void __launch_bounds__(256)
+    permute_scan_kernel(const int32_t *__restrict__ counts, int nchunks, int E,
+                        int32_t *__restrict__ bases, int32_t *__restrict__ offsets) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E)
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = counts[(size_t)c * E + e];
+      bases[(size_t)c * E + e] = total;
+      total += v;
+    }
+  const int start = block_exclusive_scan(e < E ? total : 0, warp_sums);
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) bases[(size_t)c * E + e] += start;
+    offsets[e] = start;
+    if (e == E - 1) offsets[E] = start + total;
+  }
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+    permute_scatter_kernel(const int32_t *__restrict__ idx, int Tk, int E,
+                           const int32_t *__restrict__ bases, int32_t *__restrict__ slot_of,
+                           int32_t *__restrict__ row_src) {
+  extern __shared__ int wcnt[];  // [32 warps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int wbase = blockIdx.x * kPermuteChunk + warp * kEntriesPerWarp;
+  int *mine = wcnt + warp * E;
+  // pass A: per-warp counts, in entry order
+  for (int sub = 0; sub < kEntriesPerWarp; sub += 32) {
+    const int n = wbase + sub + lane;
+    int e = n < Tk ? idx[n] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per expert: the chunk's base plus the counts of the warps before
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = bases[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // pass B: slot = running base + rank among equal experts in this group of 32
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int sub = 0; sub < kEntriesPerWarp; sub += 32) {
+    const int n = wbase + sub + lane;
+    int e = n < Tk ? idx[n] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int slot = -1;
+    if (e >= 0) slot = mine[e] + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+    if (n < Tk) {
+      slot_of[n] = slot;
+      if (slot >= 0) row_src[slot] = n;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    permute_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ row_src,
+                          const int32_t *__restrict__ offsets, int E, int top_k, int vec_per_row,
+                          uint4 *__restrict__ x_perm) {
+  const int rows = offsets[E];
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const int t = row_src[r] / top_k;
+    const uint4 *src = x + (size_t)t * vec_per_row;
+    uint4 *dst = x_perm + (size_t)r * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
+  }
+}
+
+}  // namespace
+
+moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
+                          int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
+                          int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream) {
+  const int Tk = d.T * d.top_k;
+  const int nchunks = std::max(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
+  static bool attr_set = false;
+  const int scatter_smem = 32 * d.E * 4;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             32 * 256 * 4) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  permute_count_kernel<<<nchunks, kChunkThreads, d.E * 4, stream>>>(topk_idx, Tk, d.E, counts,
+                                                                     status);
+  permute_scan_kernel<<<1, 256, 0, stream>>>(counts, nchunks, d.E, bases, expert_offsets);
+  permute_scatter_kernel<<<nchunks, kChunkThreads, scatter_smem, stream>>>(topk_idx, Tk, d.E, bases,
+                                                                          slot_of, row_src);
+  if (Tk > 0) {
+    const int blocks = std::max(1, std::min((Tk + 7) / 8, device_sm_count() * 8));
+    permute_gather_kernel<<<blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
+        static_cast<uint4 *>(x_perm));
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace beam

@@ -1,0 +1,294 @@
+// Router of the Beam MoE block: sigmoid scores with a per-expert selection
+// bias and group-limited top-k ("Hugging Face releases Beam ...", third
+// paragraph; "Reflection Releases Beam ...", section "Where Beam Saves and
+// Where the Memory Bill Comes In"; "Beam 1.0" for the bias).
+//
+// Three kernels:
+//   1. router_split_kernel: the fp32 router weight W is split into three bf16
+//      matrices hi + mid + lo == W exactly, laid side by side as W3 [E, 3H].
+//   2. tc_gemm_kernel<RouterLogits>: logits = x . W3^T on tcgen05 tensor
+//      cores.  x is bf16 and each part has 8 significant bits, so every
+//      product is exact in the fp32 accumulator.  For small T the K range is
+//      split over CTAs and the partial sums are added in a fixed order later.
+//   3. router_topk_kernel: one warp per token; sigmoid, bias, group top-2
+//      sums, top groups and top experts by warp shuffles in registers.
+#include "moe_internal.cuh"
+#include "tc_gemm.cuh"
+
+namespace beam {
+
+__global__ void router_split_kernel(const float *__restrict__ w, __nv_bfloat16 *__restrict__ w3,
+                                    int E, int H) {
+  const size_t n = (size_t)E * H;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / H), h = (int)(i % H);
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);  // exact: v and hi share the top bits
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);  // exact, at most 8 significant bits
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    __nv_bfloat16 *row = w3 + (size_t)e * 3 * H;
+    row[h] = hi;
+    row[H + h] = mid;
+    row[2 * H + h] = lo;
+  }
+}
+
+// logits partial sums: D[token, expert] over one K range of [x x x] . [hi mid lo]^T
+template <int BN_>
+struct RouterLogits {
+  static constexpr int BN = BN_;
+  static constexpr int NA = 1;
+  static constexpr int NBUF = 1;
+  static constexpr int STAGES = 4;
+  struct Params {
+    CUtensorMap tmap_x;   // bf16 [T, H], box {64, 128}
+    CUtensorMap tmap_w3;  // bf16 [E, 3H], box {64, BN}
+    float *partial;       // fp32 [ksplit, T, E]
+    int T, E, H, ksteps, ksplit;
+    uint32_t *status;
+  };
+  struct Sched {
+    int unused;
+  };
+  struct Tile {
+    int m0, kbeg, kend, split;
+  };
+  __device__ static void prologue(const Params &, Sched &) {}
+  __device__ static int num_tiles(const Params &, const Sched &) { return gridDim.x; }
+  __device__ static Tile tile(const Params &p, const Sched &, int t) {
+    const int s = blockIdx.y;
+    return Tile{t * kTileM, (int)((long)p.ksteps * s / p.ksplit),
+                (int)((long)p.ksteps * (s + 1) / p.ksplit), s};
+  }
+  __device__ static int num_k(const Params &, const Tile &t) { return t.kend - t.kbeg; }
+  __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
+    const int kk = t.kbeg + k;
+    const int hsteps = p.H / kTileK;
+    tma_load_2d(stage, &p.tmap_x, bar, (kk % hsteps) * kTileK, t.m0);
+    tma_load_2d(stage + kATileBytes, &p.tmap_w3, bar, kk * kTileK, 0);
+  }
+  __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
+    const int token = t.m0 + row;
+    for (int c = 0; c < BN; c += 32) {
+      if (c >= p.E) break;
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld();
+      if (token < p.T) {
+        float4 *dst = reinterpret_cast<float4 *>(p.partial + ((size_t)t.split * p.T + token) * p.E + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ top-k
+
+struct TopkArgs {
+  const float *partial;  // [ksplit, T, E]
+  const float *bias;     // [E]
+  int32_t *topk_idx;     // [T, k]
+  float *topk_w;         // [T, k]
+  int T, E, n_group, topk_group, top_k, ksplit;
+  int log2_gsize;
+  float routed_scale;
+};
+
+// Merge (a1 >= a2) with (b1 >= b2) into the two largest of the four.
+__device__ __forceinline__ void top2_merge(float &a1, float &a2, float b1, float b2) {
+  const float hi = fmaxf(a1, b1);
+  const float lo = fmaxf(fminf(a1, b1), fmaxf(a2, b2));
+  a1 = hi;
+  a2 = lo;
+}
+
+// One warp per token.  Lane l holds experts e = l + 32 i, i = 0..7.
+__global__ void __launch_bounds__(256) router_topk_kernel(TopkArgs a) {
+  constexpr int NS = 8;
+  const int lane = threadIdx.x & 31;
+  const int gsize = 1 << a.log2_gsize;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
+    float s[NS], sb[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const int e = lane + 32 * i;
+      if (e < a.E) {
+        float l = 0.f;
+        for (int sp = 0; sp < a.ksplit; ++sp) l += a.partial[((size_t)sp * a.T + t) * a.E + e];
+        s[i] = 1.0f / (1.0f + expf(-l));
+        sb[i] = s[i] + a.bias[e];
+      } else {
+        s[i] = 0.f;
+        sb[i] = -INFINITY;
+      }
+    }
+    // ---- group scores: sum of the two largest biased scores per group
+    float g1[NS], g2[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      g1[i] = sb[i];
+      g2[i] = -INFINITY;
+    }
+    const int seg = gsize < 32 ? gsize : 32;  // lanes per group inside one slot
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      if (off < seg) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+          const float o1 = __shfl_xor_sync(0xffffffffu, g1[i], off);
+          const float o2 = __shfl_xor_sync(0xffffffffu, g2[i], off);
+          top2_merge(g1[i], g2[i], o1, o2);
+        }
+      }
+    }
+    // a group wider than 32 spans gsize/32 consecutive slots: tree-merge them
+    // into the group's first slot (static register indices only)
+    if (gsize >= 64) {
+#pragma unroll
+      for (int i = 0; i < NS; i += 2) top2_merge(g1[i], g2[i], g1[i + 1], g2[i + 1]);
+    }
+    if (gsize >= 128) {
+#pragma unroll
+      for (int i = 0; i < NS; i += 4) top2_merge(g1[i], g2[i], g1[i + 2], g2[i + 2]);
+    }
+    if (gsize >= 256) top2_merge(g1[0], g2[0], g1[4], g2[4]);
+    // lane j (< n_group) fetches the score of group j
+    float my_gs = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const int first_e = lane * gsize;  // first expert of group `lane`
+      const int src = first_e & 31;
+      const float v = __shfl_sync(0xffffffffu, g1[i] + g2[i], src);
+      if (lane < a.n_group && (first_e >> 5) == i) my_gs = v;
+    }
+    // rank of group `lane`: groups with a larger score, or equal and lower index
+    int rank = 0;
+    for (int j = 0; j < a.n_group; ++j) {
+      const float v = __shfl_sync(0xffffffffu, my_gs, j);
+      if (v > my_gs || (v == my_gs && j < lane)) ++rank;
+    }
+    const uint32_t kept = __ballot_sync(0xffffffffu, lane < a.n_group && rank < a.topk_group);
+
+    // ---- top-k experts among the kept groups (descending, ties to lower index)
+    float cand[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const int e = lane + 32 * i;
+      cand[i] = (e < a.E && ((kept >> (e >> a.log2_gsize)) & 1u)) ? sb[i] : -INFINITY;
+    }
+    float wsum = 0.f, my_s = 0.f;
+    int my_e = 0;
+    for (int r = 0; r < a.top_k; ++r) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const int e = lane + 32 * i;
+        if (cand[i] > bv) {  // slots ascend in e, so a tie keeps the lower index
+          bv = cand[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      float sv = 0.f;
+      if ((be & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+          if (i == (be >> 5)) {
+            sv = s[i];
+            cand[i] = -INFINITY;
+          }
+      }
+      sv = __shfl_sync(0xffffffffu, sv, be & 31);
+      wsum += sv;
+      if (lane == r) {
+        my_s = sv;
+        my_e = be;
+      }
+    }
+    if (lane < a.top_k) {
+      a.topk_idx[(size_t)t * a.top_k + lane] = my_e;
+      a.topk_w[(size_t)t * a.top_k + lane] = a.routed_scale * my_s / wsum;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int BN>
+static moe_status launch_router_gemm(const RouterPlan &rp, const void *x, const __nv_bfloat16 *w3,
+                                     float *partial, uint32_t *status, cudaStream_t stream) {
+  using P = RouterLogits<BN>;
+  typename P::Params prm;
+  if (!make_tmap_bf16_2d(&prm.tmap_x, x, rp.H, rp.T, kTileM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&prm.tmap_w3, w3, 3 * rp.H, rp.E, BN)) return MOE_ERR_CUDA;
+  prm.partial = partial;
+  prm.T = rp.T;
+  prm.E = rp.E;
+  prm.H = rp.H;
+  prm.ksteps = 3 * rp.H / kTileK;
+  prm.ksplit = rp.ksplit;
+  prm.status = status;
+  constexpr int smem = smem_bytes_for<P>();
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  dim3 grid((rp.T + kTileM - 1) / kTileM, rp.ksplit);
+  tc_gemm_kernel<P><<<grid, 256, smem, stream>>>(prm);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_route(const moe_dims &d, const void *x, const float *w_router, const float *bias,
+                        int32_t *topk_idx, float *topk_w, const RouterPlan &rp,
+                        __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream) {
+  {
+    const size_t n = (size_t)d.E * d.H;
+    const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+    router_split_kernel<<<blocks, 256, 0, stream>>>(w_router, w3, d.E, d.H);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  moe_status st;
+  if (rp.BN == 32) st = launch_router_gemm<32>(rp, x, w3, partial, status, stream);
+  else if (rp.BN == 64) st = launch_router_gemm<64>(rp, x, w3, partial, status, stream);
+  else if (rp.BN == 128) st = launch_router_gemm<128>(rp, x, w3, partial, status, stream);
+  else st = launch_router_gemm<256>(rp, x, w3, partial, status, stream);
+  if (st != MOE_OK) return st;
+
+  TopkArgs a;
+  a.partial = partial;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.T = d.T;
+  a.E = d.E;
+  a.n_group = d.n_group;
+  a.topk_group = d.topk_group;
+  a.top_k = d.top_k;
+  a.ksplit = rp.ksplit;
+  a.log2_gsize = ilog2(d.E / d.n_group);
+  a.routed_scale = d.routed_scale;
+  const int blocks = std::max(1, std::min((d.T + 7) / 8, 148 * 16));
+  router_topk_kernel<<<blocks, 256, 0, stream>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace beam

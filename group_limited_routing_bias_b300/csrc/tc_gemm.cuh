@@ -1,0 +1,207 @@
+// Warp-specialised tcgen05 GEMM skeleton for sm_103a.
+//
+// One CTA (256 threads) per SM, persistent over tiles.  Each tile computes
+// NA accumulators D_a[128 x BN] (fp32, tensor memory) = A_a[128 x K] . B[BN x K]^T,
+// with every operand K-major bf16 staged by TMA in 64-wide K slices with the
+// 128-byte swizzle.
+//   warp 0 lane 0 : TMA producer, STAGES-deep shared-memory ring
+//   warp 1 lane 0 : MMA issuer (tcgen05.mma, M=128, N=BN, K=16 per instruction)
+//   warp 2        : tensor-memory allocation / release
+//   warps 4..7    : epilogue; warp 4+q reads accumulator rows 32q..32q+31
+// The accumulators are double-buffered in tensor memory when they fit, so
+// the epilogue of one tile overlaps the main loop of the next.
+//
+// A problem class P supplies the shapes and the tile schedule:
+//   static constexpr int BN, NA, STAGES, NBUF;
+//   struct Params { ...; uint32_t *status; };  struct Sched;  struct Tile;
+//   static void prologue(const Params&, Sched&)   (all threads; may __syncthreads)
+//   static int  num_tiles(const Params&, const Sched&)
+//   static Tile tile(const Params&, const Sched&, int t)
+//   static int  num_k(const Params&, const Tile&)
+//   static void load(const Params&, const Tile&, int k, uint8_t *stage, uint64_t *bar)
+//   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
+#pragma once
+
+#include "ptx.cuh"
+
+namespace beam {
+
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;                       // bf16 elements per 128-byte row
+constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
+constexpr int kSmemLimit = 232448;                // 227 KB dynamic shared memory
+constexpr int kSmemReserve = 4096;                // alignment slack + barriers
+
+template <int BN, int NA>
+struct StageGeom {
+  static constexpr int kBytes = NA * kATileBytes + BN * kTileK * 2;
+  static_assert(kBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+};
+
+template <class P>
+constexpr int smem_bytes_for() {
+  return kSmemReserve + P::STAGES * StageGeom<P::BN, P::NA>::kBytes + (int)sizeof(typename P::Sched);
+}
+
+template <class P>
+__global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__ typename P::Params p) {
+  constexpr int STAGE = StageGeom<P::BN, P::NA>::kBytes;
+  constexpr uint32_t kAccCols = P::NA * P::BN;
+  constexpr uint32_t kTmemCols = tmem_cols_pow2(P::NBUF * kAccCols);
+  constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, P::BN);
+  static_assert(P::NBUF * kAccCols <= 512, "accumulators exceed tensor memory");
+  static_assert(P::BN % 16 == 0 && P::BN >= 16 && P::BN <= 256, "invalid MMA N");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *stages = smem_raw + pad;
+  uint64_t *full = reinterpret_cast<uint64_t *>(stages + P::STAGES * STAGE);
+  uint64_t *empty = full + P::STAGES;
+  uint64_t *tfull = empty + P::STAGES;
+  uint64_t *tempty = tfull + P::NBUF;
+  uint64_t *drain = tempty + P::NBUF;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  typename P::Sched *sched =
+      reinterpret_cast<typename P::Sched *>(stages + P::STAGES * STAGE + 1024);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < P::NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  P::prologue(p, *sched);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = P::num_tiles(p, *sched);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t ph = 0, issued = 0, par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        const typename P::Tile tile = P::tile(p, *sched, t);
+        const int nk = P::num_k(p, tile);
+        for (int k = 0; k < nk; ++k) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE);
+          P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
+          issued |= 1u << stage;
+          par = (par & ~(1u << stage)) | (ph << stage);
+          if (++stage == P::STAGES) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every copy still in flight land before the CTA exits
+        for (int s = 0; s < P::STAGES; ++s)
+          if (issued & (1u << s)) mbar_drain_wait(&full[s], (par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0, buf = 0;
+      uint32_t ph = 0, bph = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        const typename P::Tile tile = P::tile(p, *sched, t);
+        const int nk = P::num_k(p, tile);
+        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + buf * kAccCols;
+        for (int k = 0; k < nk; ++k) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + stage * STAGE);
+          const uint64_t bdesc = umma_desc_sw128(sa + P::NA * kATileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+#pragma unroll
+            for (int a = 0; a < P::NA; ++a) {
+              const uint64_t adesc = umma_desc_sw128(sa + a * kATileBytes);
+              umma_bf16(d0 + a * P::BN, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                        (k | kk) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty[stage]);
+          any = true;
+          if (++stage == P::STAGES) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);
+        if (++buf == P::NBUF) {
+          buf = 0;
+          bph ^= 1u;
+        }
+      }
+      if (!ok && any) {  // wait for the tensor cores before the memory is released
+        umma_commit(drain);
+        mbar_drain_wait(drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t bph = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const typename P::Tile tile = P::tile(p, *sched, t);
+      bool ok = mbar_wait(&tfull[buf], bph, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * kAccCols;
+      P::epilogue(p, tile, taddr, row);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (++buf == P::NBUF) {
+        buf = 0;
+        bph ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace beam

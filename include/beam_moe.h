@@ -1,0 +1,202 @@
+/*
+ * beam_moe.h — C ABI of the B300 (sm_103a) forward pass of Beam's
+ * Mixture-of-Experts block.
+ *
+ * The layer (Reflection's Beam; "Hugging Face releases Beam ..." third
+ * paragraph, and "Reflection Releases Beam ...", section "Where Beam Saves and
+ * Where the Memory Bill Comes In"): 256 experts per layer, each a SwiGLU MLP
+ * with intermediate size 2,560, hidden size 5,120; a sigmoid router with a
+ * per-expert selection bias ("Beam 1.0", auxiliary-loss-free balancing) keeps
+ * the best 4 of 8 groups of 32 experts and picks the top 8 experts inside
+ * them; the routed weights are normalised and scaled by 2.5; no shared expert.
+ *
+ * Conventions for every call below
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     16-byte aligned (256 recommended), row-major and densely packed.  The
+ *     caller owns every buffer; the library allocates no device memory and
+ *     keeps no pointer after a call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and never synchronise, except moe_workspace_status.
+ *   - Argument errors return before anything is launched.  A failed launch
+ *     returns MOE_ERR_CUDA.  Errors found on the device (an expert index out of
+ *     range, an internal wait that ran past its time limit) set bits in the
+ *     status word at the start of the workspace; read it with
+ *     moe_workspace_status after the stream has finished.
+ *   - Workspaces must be at least moe_workspace_size(...) bytes and their
+ *     first 256 bytes zeroed once before first use (moe_workspace_init).
+ *     A workspace may be reused by consecutive calls on one stream; calls
+ *     that run concurrently need separate workspaces.
+ *   - Shape limits: H % 128 == 0, I % 128 == 0, E <= 256 with E % 32 == 0,
+ *     E % n_group == 0, group size E / n_group a power of two >= 2,
+ *     n_group <= 32, 1 <= topk_group <= n_group, 1 <= top_k <= 16 and
+ *     top_k <= topk_group * group size, 0 <= T and T * top_k < 2^31.
+ *   - T == 0 is a no-op: the call returns MOE_OK after checking the dims and
+ *     reads no pointer.
+ *   - Inputs must be finite.  Selection compares fp32 scores; equal scores go
+ *     to the lower group index, then to the lower expert index.
+ *
+ * Layouts (T tokens, H hidden, E experts, I intermediate, k = top_k)
+ *   x           bf16  [T, H]
+ *   w_router    fp32  [E, H]            one row per expert
+ *   bias        fp32  [E]               selection bias (selection only)
+ *   topk_idx    int32 [T, k]            descending biased score
+ *   topk_w      fp32  [T, k]            routed weights, sum to routed_scale
+ *   expert_offsets int32 [E + 1]        rows of expert e are
+ *                                       [offsets[e], offsets[e+1]) in the
+ *                                       permuted order
+ *   slot_of     int32 [T * k]           permuted row of entry t*k + j
+ *   row_src     int32 [T * k]           entry t*k + j held by permuted row r
+ *   x_perm      bf16  [T * k, H]        x rows in permuted (expert-major,
+ *                                       then entry-ascending) order
+ *   y_partial   bf16  [T * k, H]        routed-weight-scaled expert output
+ *                                       per permuted row
+ *   y           bf16  [T, H]            block output
+ *   bf16 experts: w_gate, w_up [E, I, H]; w_down [E, H, I]   (out x in)
+ *   NVFP4 experts: w_* packed e2m1 uint8 [E, N, K/2] with the even k in the
+ *                  low nibble, s_* e4m3 uint8 [E, N, K/16] (one scale per 16
+ *                  consecutive k), g_* fp32 [E] global scales; the weight is
+ *                  e2m1 * e4m3 * global.  (N, K) = (I, H) for gate and up,
+ *                  (H, I) for down.
+ */
+#ifndef BEAM_MOE_H
+#define BEAM_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* null/misaligned pointer or bad shape        */
+  MOE_ERR_UNSUPPORTED = 2,     /* shape outside the limits above              */
+  MOE_ERR_WORKSPACE = 3,       /* workspace missing or too small              */
+  MOE_ERR_CUDA = 4,            /* a CUDA call or kernel launch failed         */
+  MOE_ERR_DEVICE = 5,          /* the workspace status word is non-zero       */
+  MOE_ERR_NOT_IMPLEMENTED = 6
+} moe_status;
+
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wdtype;
+
+/* Which entry point a workspace is sized for. */
+typedef enum {
+  MOE_OP_ROUTE = 0,
+  MOE_OP_PERMUTE = 1,
+  MOE_OP_EXPERTS = 2,
+  MOE_OP_FORWARD = 3
+} moe_op;
+
+/* Bits of the device status word (first 4 bytes of a workspace). */
+#define MOE_DEV_TIMEOUT 0x1   /* an internal wait ran past its limit        */
+#define MOE_DEV_BAD_INDEX 0x2 /* an expert index outside [0, E) was skipped */
+
+typedef struct {
+  int T;              /* tokens in this call                               */
+  int H;              /* hidden size (Beam: 5120)                          */
+  int E;              /* routed experts (Beam: 256)                        */
+  int n_group;        /* expert groups (Beam: 8)                           */
+  int topk_group;     /* groups kept per token (Beam: 4)                   */
+  int top_k;          /* experts per token (Beam: 8)                       */
+  int I;              /* SwiGLU intermediate size (Beam: 2560)             */
+  float routed_scale; /* factor on the normalised weights (Beam: 2.5)      */
+} moe_dims;
+
+typedef struct {
+  moe_wdtype dtype;
+  const void *w_gate, *w_up, *w_down;    /* bf16, or packed e2m1 (NVFP4)  */
+  const uint8_t *s_gate, *s_up, *s_down; /* e4m3 block scales (NVFP4 only) */
+  const float *g_gate, *g_up, *g_down;   /* fp32 [E] global (NVFP4 only)   */
+} moe_experts;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int moe_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_string(moe_status s);
+
+/* Checks dims against the shape limits above; MOE_OK if supported. */
+moe_status moe_check_dims(const moe_dims *dims);
+
+/* Bytes of workspace that entry point `op` needs for these dims (0 if the
+ * dims are unsupported).  Includes the 256-byte status header. */
+size_t moe_workspace_size(const moe_dims *dims, moe_wdtype wdtype, moe_op op);
+
+/* Zeroes the 256-byte status header of a workspace (asynchronous). */
+moe_status moe_workspace_init(void *ws, moe_stream_t stream);
+
+/* Synchronises `stream`, then copies the workspace status word into
+ * *out_bits (0 = no device error).  Returns MOE_ERR_DEVICE if it is set. */
+moe_status moe_workspace_status(const void *ws, moe_stream_t stream, uint32_t *out_bits);
+
+/*
+ * Router: sigmoid scores, per-expert selection bias, group-limited top-k.
+ * ("Hugging Face releases Beam ...", third paragraph: top 8 experts from the
+ * top 4 of 8 groups of 32; "Reflection Releases Beam ...", section "Where Beam
+ * Saves ...": sigmoid scores, DeepSeek-V3 group limits, normalised and scaled
+ * by 2.5; "Beam 1.0": per-expert bias of auxiliary-loss-free balancing.)
+ *   logit[t,e] = sum_h x[t,h] * w_router[e,h]      (fp32 accumulation)
+ *   s = sigmoid(logit); s' = s + bias[e]           (s' selects, s weighs)
+ *   group score = sum of the two largest s' of the group
+ *   keep the topk_group best groups; take the top_k largest s' among their
+ *   experts; topk_w = routed_scale * s / sum of the chosen s.
+ * Outputs topk_idx [T,k] and topk_w [T,k].  Workspace: MOE_OP_ROUTE.
+ */
+moe_status moe_route(const moe_dims *dims, const void *x, const float *w_router,
+                     const float *bias, int32_t *topk_idx, float *topk_w, void *ws,
+                     size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Dispatch: sorts the T*k (token, slot) entries by expert, stably (entries of
+ * one expert keep ascending t*k + j order), and gathers x rows into that order.
+ * (The pages: tokens must reach the experts they selected — "Beam Turns
+ * Frontier-Scale Openness Into an Infrastructure Decision", section "Sparse
+ * compute still requires dense planning".)
+ * Outputs expert_offsets [E+1], slot_of [T*k], row_src [T*k], x_perm [T*k,H].
+ * Entries with an index outside [0,E) set MOE_DEV_BAD_INDEX and are dropped.
+ * Workspace: MOE_OP_PERMUTE.
+ */
+moe_status moe_permute(const moe_dims *dims, const int32_t *topk_idx, const void *x,
+                       void *x_perm, int32_t *expert_offsets, int32_t *slot_of,
+                       int32_t *row_src, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Expert MLPs over the permuted rows ("Hugging Face releases Beam ...", third
+ * paragraph: each expert a SwiGLU MLP with intermediate size 2,560):
+ *   h = silu(x_perm . W_gate[e]^T) * (x_perm . W_up[e]^T)     (h kept in bf16)
+ *   y_partial[r] = topk_w[row_src[r]] * (h . W_down[e]^T)      (stored bf16)
+ * for every permuted row r of expert e.  fp32 accumulation on tensor cores.
+ * topk_w is indexed by entry (t*k + j).  Workspace: MOE_OP_EXPERTS.
+ */
+moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts,
+                              const void *x_perm, const int32_t *expert_offsets,
+                              const int32_t *row_src, const float *topk_w, void *y_partial,
+                              void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Combine: y[t] = sum over j = 0..k-1, in that order, of y_partial[slot_of[t*k+j]],
+ * summed in fp32 and rounded once to bf16.  No shared expert enters the sum
+ * ("Reflection Releases Beam ...", section "Where Beam Saves ...": there is no
+ * shared expert).  Deterministic.  Needs no workspace.
+ */
+moe_status moe_combine(const moe_dims *dims, const void *y_partial, const int32_t *slot_of,
+                       void *y, moe_stream_t stream);
+
+/*
+ * The whole block: moe_route, moe_permute, moe_experts_swiglu and moe_combine
+ * in sequence on `stream`, with every intermediate in the workspace.
+ * topk_idx / topk_w may be NULL; when given they receive the routing.
+ * Workspace: MOE_OP_FORWARD.
+ */
+moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_router,
+                       const float *bias, const moe_experts *experts, void *y, int32_t *topk_idx,
+                       float *topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAM_MOE_H */

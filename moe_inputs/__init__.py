@@ -59,7 +59,7 @@ BEAM = dict(H=5120, E=256, n_group=8, topk_group=4, top_k=8, I=2560, routed_scal
 # r^-1.1 over a seeded random expert permutation.  It was chosen so that the
 # most-loaded expert receives about 8x the mean load at T=16384 with seed 0;
 # tests/golden/derive_skew_alpha.py recomputes it with the oracle's router.
-SKEW_ALPHA = 0.0525
+SKEW_ALPHA = 0.0437
 
 CONFIGS = {
     "tiny": MoeConfig("tiny", T=64, H=256, E=32, n_group=8, topk_group=2, top_k=4, I=128),
@@ -102,18 +102,32 @@ def make_router_inputs(cfg: MoeConfig, seed: int = 0, T: Optional[int] = None):
     return x.contiguous(), w_router.to(torch.float32).contiguous(), bias.to(torch.float32).contiguous()
 
 
-def make_expert_weights(cfg: MoeConfig, device="cpu", seed: int = 0):
-    """bf16 W_gate [E,I,H], W_up [E,I,H], W_down [E,H,I], drawn expert by expert on ``device``."""
-    E, H, I = cfg.E, cfg.H, cfg.I
+def _expert_seed(seed: int, matrix: int, e: int) -> int:
+    return 1_000_003 * (seed + 1) + 4099 * matrix + e
+
+
+def make_expert(cfg: MoeConfig, e: int, device="cpu", seed: int = 0):
+    """bf16 (W_gate [I,H], W_up [I,H], W_down [H,I]) of expert e alone, each
+    drawn from its own seeded generator on ``device``."""
+    H, I = cfg.H, cfg.I
     out = []
     for j, (shape, fan_in) in enumerate((((I, H), H), ((I, H), H), ((H, I), I))):
-        w = torch.empty((E,) + shape, dtype=torch.bfloat16, device=device)
-        g = _gen(seed + 11 + j, device)
-        std = 1.0 / math.sqrt(fan_in)
-        for e in range(E):
-            w[e] = (torch.randn(shape, generator=g, device=device) * std).to(torch.bfloat16)
-        out.append(w)
+        g = _gen(_expert_seed(seed, j, e), device)
+        w = torch.randn(shape, generator=g, device=device) * (1.0 / math.sqrt(fan_in))
+        out.append(w.to(torch.bfloat16))
     return tuple(out)
+
+
+def make_expert_weights(cfg: MoeConfig, device="cpu", seed: int = 0):
+    """bf16 W_gate [E,I,H], W_up [E,I,H], W_down [E,H,I], drawn expert by expert on ``device``
+    (expert e holds the same values as ``make_expert(cfg, e, device, seed)``)."""
+    E, H, I = cfg.E, cfg.H, cfg.I
+    wg = torch.empty((E, I, H), dtype=torch.bfloat16, device=device)
+    wu = torch.empty((E, I, H), dtype=torch.bfloat16, device=device)
+    wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        wg[e], wu[e], wd[e] = make_expert(cfg, e, device, seed)
+    return wg, wu, wd
 
 
 # ---------------------------------------------------------------- NVFP4 packing (data preparation)

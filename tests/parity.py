@@ -1,0 +1,109 @@
+"""Parity helpers shared by the GPU tests and the benchmark: routing comparison
+with near-tie accounting, and the output error norms.
+
+Rule for routing: expert indices must match the oracle exactly, except for
+tokens where the oracle's decision is a near tie: the gap between the
+kept/dropped groups (topk_group-th vs next group score) or between any two
+neighbours among the top_k + 1 best candidate biased scores is below 1e-5.
+Such tokens are counted; the GPU's choice is accepted for them when its total
+biased score is within top_k * 1e-5 of the oracle's, and their reference
+output is then computed with the GPU's indices (weights from the oracle's
+unbiased scores).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+TIE_EPS = 1e-5
+W_RTOL = 2e-6
+BF16_MAX_ERR = 2e-2      # max |err| <= 2e-2 * max |ref|
+BF16_REL_FROB = 5e-3     # ||err|| <= 5e-3 * ||ref||
+NVFP4_REL_FROB = 3e-2
+
+
+@dataclass
+class RoutingReport:
+    tokens: int
+    flagged: int
+    flagged_differing: int
+    mismatched: int                      # unflagged tokens whose indices differ
+    weight_max_rel: float
+    use_gpu: np.ndarray = field(repr=False)  # bool [T]: reference uses the GPU's indices
+
+    @property
+    def ok(self) -> bool:
+        return self.mismatched == 0 and self.weight_max_rel <= W_RTOL
+
+
+def near_tie_mask(orc, n_group, topk_group, top_k, eps=TIE_EPS) -> np.ndarray:
+    T, E = orc.biased.shape
+    gsz = E // n_group
+    gs = -np.sort(-orc.group_score.astype(np.float64), axis=1)
+    group_gap = (gs[:, topk_group - 1] - gs[:, topk_group]) if topk_group < n_group \
+        else np.full(T, np.inf)
+    kept_e = np.repeat(orc.group_kept.astype(bool), gsz, axis=1)
+    cand = np.where(kept_e, orc.biased.astype(np.float64), -np.inf)
+    top = -np.sort(-cand, axis=1)[:, :top_k + 1]
+    gaps = top[:, :-1] - top[:, 1:]
+    gaps = np.where(np.isfinite(gaps), gaps, np.inf)
+    return np.minimum(group_gap, gaps.min(axis=1)) < eps
+
+
+def compare_routing(orc, gpu_idx, gpu_w, n_group, topk_group, top_k, routed_scale) -> RoutingReport:
+    gpu_idx = np.asarray(gpu_idx)
+    gpu_w = np.asarray(gpu_w)
+    T, E = orc.biased.shape
+    flagged = near_tie_mask(orc, n_group, topk_group, top_k)
+    same = np.all(gpu_idx == orc.idx, axis=1)
+    mismatched = int(np.sum(~same & ~flagged))
+    use_gpu = ~same & flagged
+    for t in np.nonzero(use_gpu)[0]:
+        g = gpu_idx[t]
+        ok = len(set(g.tolist())) == top_k and np.all((g >= 0) & (g < E))
+        if ok:
+            obj_gpu = orc.biased[t, g].astype(np.float64).sum()
+            obj_orc = orc.biased[t, orc.idx[t]].astype(np.float64).sum()
+            ok = abs(obj_gpu - obj_orc) <= top_k * TIE_EPS
+        if not ok:
+            mismatched += 1
+            use_gpu[t] = False
+    # weights: against the oracle's unbiased scores for whichever indices are used
+    ref_w = orc.w.astype(np.float64).copy()
+    for t in np.nonzero(use_gpu)[0]:
+        s = orc.scores[t, gpu_idx[t]].astype(np.float64)
+        ref_w[t] = routed_scale * s / s.sum()
+    good = same | use_gpu
+    rel = np.abs(gpu_w.astype(np.float64) - ref_w) / np.abs(ref_w)
+    wmax = float(rel[good].max()) if good.any() else 0.0
+    return RoutingReport(T, int(flagged.sum()), int(use_gpu.sum()), mismatched, wmax, use_gpu)
+
+
+def reference_routing(orc, report: RoutingReport, gpu_idx, routed_scale):
+    """Indices and weights the reference output is computed with."""
+    idx = orc.idx.copy()
+    w = orc.w.copy()
+    for t in np.nonzero(report.use_gpu)[0]:
+        idx[t] = gpu_idx[t]
+        s = orc.scores[t, gpu_idx[t]].astype(np.float64)
+        w[t] = (routed_scale * s / s.sum()).astype(np.float32)
+    return idx, w
+
+
+@dataclass
+class OutputErrors:
+    max_abs: float
+    ref_max: float
+    rel_frob: float
+
+    def ok(self, max_rel=BF16_MAX_ERR, frob=BF16_REL_FROB) -> bool:
+        return self.max_abs <= max_rel * self.ref_max and self.rel_frob <= frob
+
+
+def output_errors(y_gpu, y_ref) -> OutputErrors:
+    a = np.asarray(y_gpu, np.float64)
+    b = np.asarray(y_ref, np.float64)
+    err = a - b
+    return OutputErrors(float(np.abs(err).max()), float(np.abs(b).max()),
+                        float(np.linalg.norm(err) / np.linalg.norm(b)))

@@ -52,3 +52,12 @@ def test_nvfp4_pack_roundtrip_of_representable_matrix():
     sv = s.view(torch.float8_e4m3fn).to(torch.float32).repeat_interleave(16, dim=1)
     back = mag * sv * g
     torch.testing.assert_close(back, w.to(torch.float32), rtol=1e-2, atol=0)
+
+
+def test_expert_weights_are_per_expert_seeded():
+    cfg = mi.CONFIGS["tiny"]
+    wg, wu, wd = mi.make_expert_weights(cfg, seed=2)
+    g5, u5, d5 = mi.make_expert(cfg, 5, seed=2)
+    assert torch.equal(wg[5], g5) and torch.equal(wu[5], u5) and torch.equal(wd[5], d5)
+    assert not torch.equal(wg[5], wg[6])
+    assert abs(float(wd.float().std()) * np.sqrt(cfg.I) - 1.0) < 0.02
