@@ -105,7 +105,7 @@ class ClockSampler:
 class Workload:
     """Seeded inputs of one workload resident on the GPU, plus buffers."""
 
-    def __init__(self, lib, cfg, weights, dev):
+    def __init__(self, lib, cfg, weights, dev, stages=True):
         import moe_inputs as mi
         self.cfg = cfg
         self.d = lib.dims_of(cfg)
@@ -119,6 +119,8 @@ class Workload:
         self.idx = torch.empty(T, k, dtype=torch.int32, device=dev)
         self.w = torch.empty(T, k, dtype=torch.float32, device=dev)
         self.y_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        if not stages:
+            return
         Tk = T * k
         self.x_perm = torch.empty(Tk, H, dtype=torch.bfloat16, device=dev)
         self.offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
@@ -273,6 +275,33 @@ def run_reference(args, peaks):
 # ---------------------------------------------------------------- main
 
 
+def profile_config(name):
+    """Workloads for --profile: the three full-size ones, and two small cases
+    (32 experts, 2.5 GB of weights) that keep ncu captures to a few GB."""
+    import moe_inputs as mi
+    small = dict(H=5120, E=32, n_group=8, topk_group=4, top_k=8, I=2560, routed_scale=2.5)
+    extra = {"prefill-small": mi.MoeConfig("prefill-small", T=4096, bias="zero", **small),
+             "decode-small": mi.MoeConfig("decode-small", T=64, **small)}
+    return extra[name] if name in extra else mi.CONFIGS[name]
+
+
+def run_profile(args):
+    """Only W + K moe_forward calls of one workload (the command ncu captures)."""
+    import group_limited_routing_bias_b300 as lib
+    import moe_inputs as mi
+    dev = torch.device("cuda", 0)
+    cfg = profile_config(args.profile)
+    weights = mi.make_expert_weights(cfg, device=dev)
+    wl = Workload(lib, cfg, weights, dev, stages=False)
+    for _ in range(args.warmup):
+        wl.forward(lib)
+    torch.cuda.synchronize()
+    per = time_steps(lambda: wl.forward(lib), args.steps, lambda: None)
+    assert lib.workspace_status(wl.ws) == 0
+    print(json.dumps({"profile": args.profile, "T": cfg.T, "E": cfg.E, "steps": args.steps,
+                      "ms_per_step": statistics.mean(per)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -282,8 +311,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--profile", choices=["decode", "prefill", "skewed", "prefill-small",
+                                          "decode-small"], default=None,
+                    help="run only warm-up + steps forwards of one workload (for ncu)")
     args = ap.parse_args()
     peaks = load_peaks()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args, peaks)
         return
