@@ -20,11 +20,6 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
 
-if not os.path.exists(LIB_PATH):
-    raise ImportError(
-        f"{LIB_PATH} is missing; build it with `python -m group_limited_routing_bias_b300.build`")
-_lib = ctypes.CDLL(LIB_PATH)
-
 MOE_OK = 0
 MOE_W_BF16, MOE_W_NVFP4 = 0, 1
 MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_EXPERTS, MOE_OP_FORWARD = 0, 1, 2, 3
@@ -63,10 +58,24 @@ _sig = {
     "moe_combine": ([_DP, _P, _P, _P, _P], _I),
     "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
 }
-for _name, (_args, _ret) in _sig.items():
-    _f = getattr(_lib, _name)
-    _f.argtypes = _args
-    _f.restype = _ret
+_native = None
+
+
+def native() -> ctypes.CDLL:
+    """The loaded libbeam_moe.so.  Raises ImportError if it has not been built:
+    there is no other implementation to fall back to."""
+    global _native
+    if _native is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing; build it with "
+                              "`python -m group_limited_routing_bias_b300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, ret) in _sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ret
+        _native = lib
+    return _native
 
 
 class MoeError(RuntimeError):
@@ -76,11 +85,11 @@ class MoeError(RuntimeError):
 
 
 def status_string(status: int) -> str:
-    return _lib.moe_status_string(status).decode()
+    return native().moe_status_string(status).decode()
 
 
 def version() -> int:
-    return _lib.moe_version()
+    return native().moe_version()
 
 
 def _check(fn: str, status: int):
@@ -99,11 +108,11 @@ def dims_of(cfg, T: Optional[int] = None) -> MoeDims:
 
 
 def check_dims(d: MoeDims) -> int:
-    return _lib.moe_check_dims(ctypes.byref(d))
+    return native().moe_check_dims(ctypes.byref(d))
 
 
 def workspace_size(d: MoeDims, op: int, wdtype: int = MOE_W_BF16) -> int:
-    return _lib.moe_workspace_size(ctypes.byref(d), wdtype, op)
+    return native().moe_workspace_size(ctypes.byref(d), wdtype, op)
 
 
 def alloc_workspace(d: MoeDims, op: int, wdtype: int = MOE_W_BF16, device="cuda") -> torch.Tensor:
@@ -137,14 +146,14 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, shape=None, name="tensor"):
 def workspace_status(ws: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the workspace's device status bits."""
     bits = ctypes.c_uint32(0)
-    st = _lib.moe_workspace_status(_ptr(ws, torch.uint8, name="ws"), _stream(stream), ctypes.byref(bits))
+    st = native().moe_workspace_status(_ptr(ws, torch.uint8, name="ws"), _stream(stream), ctypes.byref(bits))
     if st not in (MOE_OK, 5):
         raise MoeError("moe_workspace_status", st)
     return bits.value
 
 
 def workspace_init(ws: torch.Tensor, stream=None):
-    _check("moe_workspace_init", _lib.moe_workspace_init(_ptr(ws, torch.uint8, name="ws"), _stream(stream)))
+    _check("moe_workspace_init", native().moe_workspace_init(_ptr(ws, torch.uint8, name="ws"), _stream(stream)))
 
 
 @dataclass
@@ -191,7 +200,7 @@ class Experts:
 def moe_route(d: MoeDims, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
     """Router; fills topk_idx int32 [T,k] and topk_w fp32 [T,k]."""
     T, H, E, k = d.T, d.H, d.E, d.top_k
-    _check("moe_route", _lib.moe_route(
+    _check("moe_route", native().moe_route(
         ctypes.byref(d), _ptr(x, torch.bfloat16, (T, H), "x"),
         _ptr(w_router, torch.float32, (E, H), "w_router"), _ptr(bias, torch.float32, (E,), "bias"),
         _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
@@ -201,7 +210,7 @@ def moe_route(d: MoeDims, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
 def moe_permute(d: MoeDims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src, ws, stream=None):
     """Dispatch; fills expert_offsets [E+1], slot_of [T*k], row_src [T*k], x_perm [T*k, H]."""
     T, H, E, Tk = d.T, d.H, d.E, d.T * d.top_k
-    _check("moe_permute", _lib.moe_permute(
+    _check("moe_permute", native().moe_permute(
         ctypes.byref(d), _ptr(topk_idx, torch.int32, (T, d.top_k), "topk_idx"),
         _ptr(x, torch.bfloat16, (T, H), "x"), _ptr(x_perm, torch.bfloat16, (Tk, H), "x_perm"),
         _ptr(expert_offsets, torch.int32, (E + 1,), "expert_offsets"),
@@ -214,7 +223,7 @@ def moe_experts_swiglu(d: MoeDims, experts: Experts, x_perm, expert_offsets, row
     """Expert SwiGLU MLPs over permuted rows; fills y_partial bf16 [T*k, H]."""
     Tk, H, E = d.T * d.top_k, d.H, d.E
     ex = experts.struct(d)
-    _check("moe_experts_swiglu", _lib.moe_experts_swiglu(
+    _check("moe_experts_swiglu", native().moe_experts_swiglu(
         ctypes.byref(d), ctypes.byref(ex), _ptr(x_perm, torch.bfloat16, (Tk, H), "x_perm"),
         _ptr(expert_offsets, torch.int32, (E + 1,), "expert_offsets"),
         _ptr(row_src, torch.int32, (Tk,), "row_src"),
@@ -226,7 +235,7 @@ def moe_experts_swiglu(d: MoeDims, experts: Experts, x_perm, expert_offsets, row
 def moe_combine(d: MoeDims, y_partial, slot_of, y, stream=None):
     """Deterministic combine; fills y bf16 [T, H]."""
     Tk, H = d.T * d.top_k, d.H
-    _check("moe_combine", _lib.moe_combine(
+    _check("moe_combine", native().moe_combine(
         ctypes.byref(d), _ptr(y_partial, torch.bfloat16, (Tk, H), "y_partial"),
         _ptr(slot_of, torch.int32, (Tk,), "slot_of"), _ptr(y, torch.bfloat16, (d.T, H), "y"),
         _stream(stream)))
@@ -237,9 +246,10 @@ def moe_forward(d: MoeDims, x, w_router, bias, experts: Experts, y, ws, topk_idx
     """The whole block; fills y bf16 [T, H] (and the routing, when given buffers)."""
     T, H, E, k = d.T, d.H, d.E, d.top_k
     ex = experts.struct(d)
-    _check("moe_forward", _lib.moe_forward(
+    _check("moe_forward", native().moe_forward(
         ctypes.byref(d), _ptr(x, torch.bfloat16, (T, H), "x"),
         _ptr(w_router, torch.float32, (E, H), "w_router"), _ptr(bias, torch.float32, (E,), "bias"),
         ctypes.byref(ex), _ptr(y, torch.bfloat16, (T, H), "y"),
         _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
         _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
+

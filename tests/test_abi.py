@@ -77,7 +77,7 @@ def test_argument_errors_return_before_launch(lib):
     P = ctypes.c_void_p
     fake = P(1 << 20)        # never dereferenced: the checks fail first
     mis = P((1 << 20) + 4)   # misaligned
-    so = lib._lib
+    so = lib.native()
     ws_n = lib.workspace_size(d, lib.MOE_OP_ROUTE)
     # null pointer
     assert so.moe_route(ctypes.byref(d), None, fake, fake, fake, fake, fake, ws_n, None) == 1
