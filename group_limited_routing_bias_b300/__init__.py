@@ -27,7 +27,7 @@ MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
 
 EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
             "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
-            "moe_experts_swiglu", "moe_combine", "moe_forward")
+            "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_permute_noalloc")
 
 
 class MoeDims(ctypes.Structure):
@@ -57,6 +57,7 @@ _sig = {
     "moe_experts_swiglu": ([_DP, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "moe_combine": ([_DP, _P, _P, _P, _P], _I),
     "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
+    "moe_permute_noalloc": ([_DP, _P, _P, _P, _P, _P, _P, _P], _I),
 }
 _native = None
 
@@ -253,3 +254,16 @@ def moe_forward(d: MoeDims, x, w_router, bias, experts: Experts, y, ws, topk_idx
         _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
         _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
 
+
+def moe_permute_noalloc(d: MoeDims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src,
+                        stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device
+    memory (the scratch is a fixed 1 MiB array inside the library; concurrent
+    calls race, see include/beam_moe.h)."""
+    T, H, E, Tk = d.T, d.H, d.E, d.T * d.top_k
+    _check("moe_permute_noalloc", native().moe_permute_noalloc(
+        ctypes.byref(d), _ptr(topk_idx, torch.int32, (T, d.top_k), "topk_idx"),
+        _ptr(x, torch.bfloat16, (T, H), "x"), _ptr(x_perm, torch.bfloat16, (Tk, H), "x_perm"),
+        _ptr(expert_offsets, torch.int32, (E + 1,), "expert_offsets"),
+        _ptr(slot_of, torch.int32, (Tk,), "slot_of"), _ptr(row_src, torch.int32, (Tk,), "row_src"),
+        _stream(stream)))

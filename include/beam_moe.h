@@ -195,6 +195,30 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
                        const float *bias, const moe_experts *experts, void *y, int32_t *topk_idx,
                        float *topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * moe_permute_noalloc — the dispatch of moe_permute for callers that cannot
+ * allocate device memory at all: a plug-in inside a host framework that owns
+ * every device buffer and passes it only its inputs and outputs, or a serving
+ * loop that forbids allocations after start-up (cudaMalloc may synchronise the
+ * device).  The pages have no counterpart to this entry point.
+ *   Same inputs, outputs and layouts as moe_permute, but no workspace: its
+ *   scratch (per-chunk expert counts and bases) lives in one 1 MiB device
+ *   array inside the library, which every GPU that loads the library holds
+ *   until the process exits.
+ *   Limit: 256 + 2 * 4 * E * ceil(T*k / 4096) bytes must fit in 1 MiB, i.e.
+ *   T*k <= 2,093,056 entries at E = 256; larger calls return
+ *   MOE_ERR_UNSUPPORTED before launching anything.
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other host threads) race and corrupt each other's results.
+ *   Out-of-range expert indices are dropped as in moe_permute, but no status
+ *   word is kept: check expert_offsets[E] == T*k instead.
+ */
+moe_status moe_permute_noalloc(const moe_dims *dims, const int32_t *topk_idx, const void *x,
+                               void *x_perm, int32_t *expert_offsets, int32_t *slot_of,
+                               int32_t *row_src, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
