@@ -139,6 +139,144 @@ struct ExpertGemm {
   }
 };
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+struct TokenMajorSched {
+  int off[257];  // expert row offsets
+  int tp[257];   // prefix of tiles per expert (token tiles x feature tiles)
+};
+
+// Token-major expert GEMM for large batches: 128 token rows of one expert on
+// the MMA's M side, 256 weight rows on the N side.  Gate/up: the N side is the
+// 128 gate rows and the 128 up rows of the same 128 features, so each thread
+// of the epilogue owns one token row and holds both g and u of its features;
+// it writes h as 16-byte vectors.  Down: 256 output features per tile, the
+// row's routing weight is one scalar per thread.  Two 256-column accumulators
+// double-buffer the 512 tensor-memory columns.  Tiles of one expert run
+// feature-tile-major so the token tiles that share a weight tile are
+// scheduled side by side and read it from L2.
+template <bool GATEUP>
+struct ExpertGemmTM {
+  static constexpr int BN = 256;
+  static constexpr int NA = 1;
+  static constexpr int NBUF = 2;
+  static constexpr int STAGES = 4;
+  static constexpr int FW = GATEUP ? 128 : 256;  // output features per tile
+
+  struct Params {
+    CUtensorMap tmap_a;   // token rows [Tk, K]: x_perm or h, box {64, 128}
+    CUtensorMap tmap_b0;  // W_gate [E*I, H] box {64,128}, or W_down [E*H, I] box {64,256}
+    CUtensorMap tmap_b1;  // W_up [E*I, H] box {64,128} (gate/up only)
+    const int32_t *offsets;
+    const int32_t *row_src;
+    const float *topk_w;
+    __nv_bfloat16 *out;  // h [Tk, I] or y_partial [Tk, H]
+    int E, out_cols, b_rows, ksteps, nf;
+    uint32_t *status;
+  };
+  using Sched = TokenMajorSched;
+  struct Tile {
+    int row0, nrows, brow0, f;
+  };
+
+  __device__ static void prologue(const Params &p, Sched &s) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.off[i] = p.offsets[i];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const int per = (p.E + 31) / 32;
+      const int e0 = lane * per;
+      int local = 0;
+      for (int e = e0; e < e0 + per && e < p.E; ++e)
+        local += (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM * p.nf;
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - local;
+      for (int e = e0; e < e0 + per && e < p.E; ++e) {
+        s.tp[e] = run;
+        run += (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM * p.nf;
+      }
+      if (lane == 31) s.tp[p.E] = incl;
+    }
+    __syncthreads();
+  }
+  __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E]; }
+  __device__ static Tile tile(const Params &p, const Sched &s, int t) {
+    int lo = 0, hi = p.E;  // last e with tp[e] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.tp[mid] <= t) lo = mid;
+      else hi = mid;
+    }
+    const int e = lo;
+    const int ntt = (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM;
+    const int local = t - s.tp[e];
+    const int f = local / ntt, tt = local - f * ntt;
+    const int row0 = s.off[e] + tt * kTileM;
+    return Tile{row0, min(kTileM, s.off[e + 1] - row0), e * p.b_rows + f * FW, f};
+  }
+  __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
+  __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
+    tma_load_2d(stage, &p.tmap_a, bar, k * kTileK, t.row0);
+    if (GATEUP) {
+      tma_load_2d(stage + kATileBytes, &p.tmap_b0, bar, k * kTileK, t.brow0);
+      tma_load_2d(stage + 2 * kATileBytes, &p.tmap_b1, bar, k * kTileK, t.brow0);
+    } else {
+      tma_load_2d(stage + kATileBytes, &p.tmap_b0, bar, k * kTileK, t.brow0);
+    }
+  }
+  __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
+    const bool valid = row < t.nrows;
+    __nv_bfloat16 *dst = p.out + (size_t)(t.row0 + row) * p.out_cols + t.f * FW;
+    if (GATEUP) {
+#pragma unroll 1
+      for (int c = 0; c < FW; c += 32) {
+        uint32_t g[32], u[32];
+        tmem_ld32(taddr + c, g);
+        tmem_ld32(taddr + FW + c, u);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+            const float h1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+            pk[j] = pack_bf16x2(h0, h1);
+          }
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    } else {
+      const float w = valid ? __ldg(p.topk_w + __ldg(p.row_src + t.row0 + row)) : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < FW; c += 32) {
+        uint32_t a[32];
+        tmem_ld32(taddr + c, a);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(a[2 * j]) * w, __uint_as_float(a[2 * j + 1]) * w);
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    }
+  }
+};
+
 template <class P>
 moe_status launch_gemm(const typename P::Params &prm, int grid, cudaStream_t stream) {
   constexpr int smem = smem_bytes_for<P>();
@@ -204,37 +342,95 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
   }
 }
 
+moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, const void *x_perm,
+                                      const int32_t *offsets, const int32_t *row_src,
+                                      const float *topk_w, void *y_partial, __nv_bfloat16 *h,
+                                      uint32_t *status, cudaStream_t stream) {
+  const long Tk = (long)d.T * d.top_k;
+  const long max_tt = Tk / kTileM + std::min<long>(d.E, Tk);
+  const int sms = device_sm_count();
+  {
+    using P = ExpertGemmTM<true>;
+    typename P::Params prm;
+    if (!make_tmap_bf16_2d(&prm.tmap_a, x_perm, d.H, Tk, kTileM) ||
+        !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_gate, d.H, (uint64_t)d.E * d.I, 128) ||
+        !make_tmap_bf16_2d(&prm.tmap_b1, ex.w_up, d.H, (uint64_t)d.E * d.I, 128))
+      return MOE_ERR_CUDA;
+    prm.offsets = offsets;
+    prm.row_src = row_src;
+    prm.topk_w = topk_w;
+    prm.out = h;
+    prm.E = d.E;
+    prm.out_cols = d.I;
+    prm.b_rows = d.I;
+    prm.ksteps = d.H / kTileK;
+    prm.nf = d.I / P::FW;
+    prm.status = status;
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.nf));
+    const moe_status st = launch_gemm<P>(prm, grid, stream);
+    if (st != MOE_OK) return st;
+  }
+  {
+    using P = ExpertGemmTM<false>;
+    typename P::Params prm;
+    if (!make_tmap_bf16_2d(&prm.tmap_a, h, d.I, Tk, kTileM) ||
+        !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_down, d.I, (uint64_t)d.E * d.H, 256))
+      return MOE_ERR_CUDA;
+    prm.tmap_b1 = prm.tmap_b0;
+    prm.offsets = offsets;
+    prm.row_src = row_src;
+    prm.topk_w = topk_w;
+    prm.out = static_cast<__nv_bfloat16 *>(y_partial);
+    prm.E = d.E;
+    prm.out_cols = d.H;
+    prm.b_rows = d.H;
+    prm.ksteps = d.I / kTileK;
+    prm.nf = d.H / P::FW;
+    prm.status = status;
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.nf));
+    return launch_gemm<P>(prm, grid, stream);
+  }
+}
+
 // ------------------------------------------------------------------ combine
 
+// One thread per (token, 8 consecutive columns): the k slot rows are loaded
+// together, summed in fp32 in slot order and rounded once to bf16.
 __global__ void __launch_bounds__(128)
     combine_kernel(const uint4 *__restrict__ y_partial, const int32_t *__restrict__ slot_of,
-                   int top_k, int vec_per_row, uint4 *__restrict__ y) {
-  __shared__ int slots[16];
-  const int t = blockIdx.x;
-  if (threadIdx.x < top_k) slots[threadIdx.x] = slot_of[(size_t)t * top_k + threadIdx.x];
-  __syncthreads();
-  for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
-    float acc[8];
+                   int T, int top_k, int vec_per_row, uint4 *__restrict__ y) {
+  const long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
+  if (i >= (long)T * vec_per_row) return;
+  const int t = (int)(i / vec_per_row), v = (int)(i % vec_per_row);
+  const int32_t *so = slot_of + (size_t)t * top_k;
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < top_k; ++j) {
-      const int s = slots[j];
-      if (s < 0) continue;
-      const uint4 q = y_partial[(size_t)s * vec_per_row + v];
-      const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&q);
+  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+  uint4 vals[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b[i]);
-        acc[2 * i] += f.x;
-        acc[2 * i + 1] += f.y;
+  for (int j = 0; j < 16; ++j) {
+    if (j < top_k) {
+      const int s = __ldg(so + j);
+      vals[j] = s >= 0 ? __ldg(y_partial + (size_t)s * vec_per_row + v) : make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < top_k) {
+      const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&vals[j]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(b[q]);
+        acc[2 * q] += f.x;
+        acc[2 * q + 1] += f.y;
       }
     }
-    uint4 o;
-    __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    y[(size_t)t * vec_per_row + v] = o;
   }
+  uint4 o;
+  __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+  y[i] = o;
 }
 
 }  // namespace
@@ -244,6 +440,10 @@ moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *
                           const float *topk_w, void *y_partial, __nv_bfloat16 *h,
                           uint32_t *status, cudaStream_t stream) {
   if (ex.dtype != MOE_W_BF16) return MOE_ERR_NOT_IMPLEMENTED;
+  const long mean_rows = ((long)d.T * d.top_k + d.E - 1) / d.E;
+  if (mean_rows >= 128 && d.H % 256 == 0)
+    return launch_experts_token_major(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h,
+                                      status, stream);
   switch (expert_bn(d)) {
     case 16: return launch_experts_bn<16>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h, status, stream);
     case 32: return launch_experts_bn<32>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h, status, stream);
@@ -256,8 +456,9 @@ moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *
 moe_status launch_combine(const moe_dims &d, const void *y_partial, const int32_t *slot_of, void *y,
                           cudaStream_t stream) {
   if (d.T == 0) return MOE_OK;
-  combine_kernel<<<d.T, 128, 0, stream>>>(static_cast<const uint4 *>(y_partial), slot_of, d.top_k,
-                                          d.H / 8, static_cast<uint4 *>(y));
+  const long n = (long)d.T * (d.H / 8);
+  combine_kernel<<<(unsigned)((n + 127) / 128), 128, 0, stream>>>(
+      static_cast<const uint4 *>(y_partial), slot_of, d.T, d.top_k, d.H / 8, static_cast<uint4 *>(y));
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -16,6 +16,7 @@ namespace beam {
 constexpr int kTargetCtas = 148;       // B300 SM count; sizes the router's K split
 constexpr int kPermuteChunk = 4096;    // entries per permute CTA (32 warps x 128)
 constexpr size_t kHeaderBytes = 256;   // workspace status header
+constexpr int kMaxRouterSplit = 20;    // router K split; the top-k kernel adds the partials
 
 inline int ilog2(int v) {
   int r = 0;
@@ -39,7 +40,7 @@ inline RouterPlan make_router_plan(const moe_dims &d) {
   p.BN = d.E <= 32 ? 32 : d.E <= 64 ? 64 : d.E <= 128 ? 128 : 256;
   const int mt = std::max(1, (d.T + 127) / 128);
   const int ksteps = 3 * d.H / 64;
-  p.ksplit = std::max(1, std::min(kTargetCtas / mt, ksteps / 4));
+  p.ksplit = std::max(1, std::min({kTargetCtas / mt, ksteps / 4, kMaxRouterSplit}));
   return p;
 }
 

@@ -116,13 +116,23 @@ __global__ void __launch_bounds__(256) router_topk_kernel(TopkArgs a) {
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
     float s[NS], sb[NS];
+    // logits: the K-split partial sums, added in split order (loads issued
+    // four splits ahead so the chain of adds does not serialise the loads)
+    float l[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) l[i] = 0.f;
+#pragma unroll 4
+    for (int sp = 0; sp < a.ksplit; ++sp) {
+      const float *row = a.partial + ((size_t)sp * a.T + t) * a.E;
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        if (lane + 32 * i < a.E) l[i] += __ldg(row + lane + 32 * i);
+    }
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const int e = lane + 32 * i;
       if (e < a.E) {
-        float l = 0.f;
-        for (int sp = 0; sp < a.ksplit; ++sp) l += a.partial[((size_t)sp * a.T + t) * a.E + e];
-        s[i] = 1.0f / (1.0f + expf(-l));
+        s[i] = 1.0f / (1.0f + expf(-l[i]));
         sb[i] = s[i] + a.bias[e];
       } else {
         s[i] = 0.f;

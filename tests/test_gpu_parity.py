@@ -184,9 +184,23 @@ def check_forward(lib, case, sample=None):
     return y, idx, w
 
 
-@pytest.mark.parametrize("T", [64, 200, 1, 5])
+@pytest.mark.parametrize("T", [64, 200, 1, 5, 1500, 2048])
 def test_forward_tiny(lib, T):
+    """Tiny shape; T >= 1500 gives >= 128 rows per expert on average, which takes
+    the token-major expert GEMMs (ragged expert tails included)."""
     check_forward(lib, Case(mi.CONFIGS["tiny"], T=T))
+
+
+def test_forward_tiny_skewed_token_major(lib):
+    """Token-major path with a strongly skewed load (some experts with one or
+    two tiles, some with many), every output compared."""
+    c = mi.CONFIGS["tiny"].with_T(1800)
+    case = Case(c)
+    case.b_h = mi.zipf_bias(c.E, 0.15, seed=3)
+    case.b = case.b_h.to(DEV)
+    y, idx, _ = check_forward(lib, case)
+    load = np.bincount(idx.ravel(), minlength=c.E)
+    assert load.max() > 3 * load.mean()
 
 
 def test_forward_decode_full(lib):
