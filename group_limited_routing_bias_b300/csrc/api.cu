@@ -35,17 +35,25 @@ bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
 }  // namespace
 
-bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
-                       uint32_t box_outer) {
+bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                  bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || outer == 0) return false;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                       uint32_t box_outer) {
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, 64, box_outer,
+                      true);
 }
 
 int device_sm_count() {
@@ -84,9 +92,10 @@ moe_status check_dims(const moe_dims *d) {
   return MOE_OK;
 }
 
-moe_status check_ws(const moe_dims *d, moe_op op, const void *ws, size_t ws_bytes) {
+moe_status check_ws(const moe_dims *d, moe_op op, const void *ws, size_t ws_bytes,
+                    moe_wdtype wdtype = MOE_W_BF16) {
   if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
-  if (ws_bytes < ws_layout(*d, op).total) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(*d, op, wdtype).total) return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
 
@@ -103,13 +112,21 @@ bool ptrs_ok(std::initializer_list<const void *> ps) {
   return true;
 }
 
-moe_status check_experts(const moe_experts *ex) {
+moe_status check_experts(const moe_dims *d, const moe_experts *ex) {
   if (!ex) return MOE_ERR_INVALID_ARG;
   if (ex->dtype == MOE_W_BF16) {
     if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down})) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
   }
-  if (ex->dtype == MOE_W_NVFP4) return MOE_ERR_NOT_IMPLEMENTED;
+  if (ex->dtype == MOE_W_NVFP4) {
+    if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down, ex->s_gate, ex->s_up, ex->s_down}))
+      return MOE_ERR_INVALID_ARG;
+    for (const float *g : {ex->g_gate, ex->g_up, ex->g_down})
+      if (!g || (reinterpret_cast<uintptr_t>(g) & 3u)) return MOE_ERR_INVALID_ARG;
+    // one TMA box of block scales spans 16 bytes = 256 k
+    if (d->H % 256 != 0 || d->I % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+  }
   return MOE_ERR_INVALID_ARG;
 }
 
@@ -138,7 +155,7 @@ size_t moe_workspace_size(const moe_dims *dims, moe_wdtype wdtype, moe_op op) {
   if (check_dims(dims) != MOE_OK) return 0;
   if (wdtype != MOE_W_BF16 && wdtype != MOE_W_NVFP4) return 0;
   if (op < MOE_OP_ROUTE || op > MOE_OP_FORWARD) return 0;
-  return ws_layout(*dims, op).total;
+  return ws_layout(*dims, op, wdtype).total;
 }
 
 moe_status moe_workspace_init(void *ws, moe_stream_t stream) {
@@ -193,13 +210,20 @@ moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts, 
   moe_status st = check_dims(dims);
   if (st != MOE_OK) return st;
   if (dims->T == 0) return MOE_OK;
-  if ((st = check_experts(experts)) != MOE_OK) return st;
+  if ((st = check_experts(dims, experts)) != MOE_OK) return st;
   if (!ptrs_ok({x_perm, expert_offsets, row_src, topk_w, y_partial})) return MOE_ERR_INVALID_ARG;
-  if ((st = check_ws(dims, MOE_OP_EXPERTS, ws, ws_bytes)) != MOE_OK) return st;
-  const WsLayout L = ws_layout(*dims, MOE_OP_EXPERTS);
+  if ((st = check_ws(dims, MOE_OP_EXPERTS, ws, ws_bytes, experts->dtype)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*dims, MOE_OP_EXPERTS, experts->dtype);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (experts->dtype == MOE_W_NVFP4) {
+    void *x16 = at<void>(ws, L.x16);
+    const size_t n = (size_t)dims->T * dims->top_k * dims->H;
+    if ((st = launch_bf16_to_f16(x_perm, x16, n, s)) != MOE_OK) return st;
+    return launch_experts_fp4(*dims, *experts, x16, expert_offsets, row_src, topk_w, y_partial,
+                              at<void>(ws, L.h), status_word(ws), s);
+  }
   return launch_experts(*dims, *experts, x_perm, expert_offsets, row_src, topk_w, y_partial,
-                        at<__nv_bfloat16>(ws, L.h), status_word(ws),
-                        reinterpret_cast<cudaStream_t>(stream));
+                        at<__nv_bfloat16>(ws, L.h), status_word(ws), s);
 }
 
 moe_status moe_combine(const moe_dims *dims, const void *y_partial, const int32_t *slot_of, void *y,
@@ -217,13 +241,14 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   moe_status st = check_dims(dims);
   if (st != MOE_OK) return st;
   if (dims->T == 0) return MOE_OK;
-  if ((st = check_experts(experts)) != MOE_OK) return st;
+  if ((st = check_experts(dims, experts)) != MOE_OK) return st;
   if (!ptrs_ok({x, w_router, bias, y})) return MOE_ERR_INVALID_ARG;
   if ((topk_idx && !aligned16(topk_idx)) || (topk_w && !aligned16(topk_w)))
     return MOE_ERR_INVALID_ARG;
-  if ((st = check_ws(dims, MOE_OP_FORWARD, ws, ws_bytes)) != MOE_OK) return st;
+  if ((st = check_ws(dims, MOE_OP_FORWARD, ws, ws_bytes, experts->dtype)) != MOE_OK) return st;
   const moe_dims &d = *dims;
-  const WsLayout L = ws_layout(d, MOE_OP_FORWARD);
+  const WsLayout L = ws_layout(d, MOE_OP_FORWARD, experts->dtype);
+  const bool fp4 = experts->dtype == MOE_W_NVFP4;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t *idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
   float *w = topk_w ? topk_w : at<float>(ws, L.topk_w);
@@ -235,13 +260,18 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   int32_t *offsets = at<int32_t>(ws, L.offsets);
   int32_t *slot_of = at<int32_t>(ws, L.slot_of);
   int32_t *row_src = at<int32_t>(ws, L.row_src);
+  // with NVFP4 weights the gather writes x_perm in f16, the GEMMs' operand type
   if ((st = launch_permute(d, idx, x, x_perm, offsets, slot_of, row_src, at<int32_t>(ws, L.counts),
-                           at<int32_t>(ws, L.bases), status, s)) != MOE_OK)
+                           at<int32_t>(ws, L.bases), status, s, fp4)) != MOE_OK)
     return st;
   void *y_partial = at<void>(ws, L.y_partial);
-  if ((st = launch_experts(d, *experts, x_perm, offsets, row_src, w, y_partial,
-                           at<__nv_bfloat16>(ws, L.h), status, s)) != MOE_OK)
-    return st;
+  if (fp4)
+    st = launch_experts_fp4(d, *experts, x_perm, offsets, row_src, w, y_partial, at<void>(ws, L.h),
+                            status, s);
+  else
+    st = launch_experts(d, *experts, x_perm, offsets, row_src, w, y_partial,
+                        at<__nv_bfloat16>(ws, L.h), status, s);
+  if (st != MOE_OK) return st;
   return launch_combine(d, y_partial, slot_of, y, s);
 }
 

@@ -60,6 +60,11 @@ struct ExpertGemm {
   struct Tile {
     int row0, nrows, arow0, m;
   };
+  static constexpr bool CONVERT = false;
+  static constexpr bool F16 = false;
+  static constexpr int RAW_BYTES = 0;
+  static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
+  __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 
   __device__ static void prologue(const Params &p, Sched &s) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.off[i] = p.offsets[i];
@@ -181,6 +186,11 @@ struct ExpertGemmTM {
   struct Tile {
     int row0, nrows, brow0, f;
   };
+  static constexpr bool CONVERT = false;
+  static constexpr bool F16 = false;
+  static constexpr int RAW_BYTES = 0;
+  static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
+  __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 
   __device__ static void prologue(const Params &p, Sched &s) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.off[i] = p.offsets[i];

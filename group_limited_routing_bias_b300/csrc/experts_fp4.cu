@@ -1,0 +1,509 @@
+// Expert MLPs with NVFP4 weights ("Reflection Releases Beam ...", section
+// "Where Beam Saves and Where the Memory Bill Comes In": an NVFP4 checkpoint
+// for Blackwell).  A weight is e2m1(code) * e4m3(block scale) * fp32 global,
+// one scale per 16 consecutive k, one global per expert and matrix.
+//
+// The activations stay 16-bit (W4A16).  The product e2m1 * e4m3 has at most
+// six significant bits and lies in [2^-10, 2688], so it is exact in f16; the
+// global scale, a per-matrix constant, is applied to the fp32 accumulator in
+// the epilogue.  The MMAs therefore run kind::f16 with f16 operands: the
+// producer TMA-loads the packed codes and their scales into a raw ring, four
+// converter warps turn each 64-wide K slice into an f16 operand tile with the
+// 128-byte swizzle (hardware e2m1x2 and e4m3x2 conversions, one f16x2
+// multiply per code pair), and the activations (exact bf16 -> f16 copies,
+// made in the dispatch gather) arrive by TMA.  h is kept in f16.
+//
+// Two tile shapes, as for bf16 weights: weights on the MMA's M side for small
+// batches (decode streams each touched expert's packed weights once), and
+// token rows on M with 256 weight rows on N for large batches.
+#include <cuda_fp16.h>
+
+#include "moe_internal.cuh"
+#include "tc_gemm.cuh"
+
+namespace beam {
+
+namespace {
+
+constexpr int kPackedRowBytes = kTileK / 2;  // 32 bytes of e2m1 pairs per row per K slice
+constexpr int kScaleBoxBytes = 16;           // one scale box: 16 scales = 256 k = 4 K slices
+constexpr int kRawRowBytes = kPackedRowBytes + kScaleBoxBytes;
+
+// One 64-wide K slice of one weight row: 32 bytes of e2m1 pairs (even k in the
+// low nibble) and the slice's four e4m3 block scales -> 64 f16 values, written
+// as eight 16-byte chunks at the 128-byte-swizzle positions of row r.
+__device__ __forceinline__ void fp4_row_to_f16(const uint8_t *packed, uint32_t scales4,
+                                               uint8_t *dst_row, int r) {
+  const uint4 p0 = *reinterpret_cast<const uint4 *>(packed);
+  const uint4 p1 = *reinterpret_cast<const uint4 *>(packed + 16);
+  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  uint32_t s2[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t b = (scales4 >> (8 * j)) & 0xFFu;
+    const uint16_t pair = (uint16_t)(b | (b << 8));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2[j]) : "h"(pair));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t o0, o1, o2, o3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+        : "r"(w[i]));
+    const uint32_t sc = s2[i >> 1];  // codes 8i..8i+7 lie in block i/2
+    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o0) : "r"(sc));
+    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o1) : "r"(sc));
+    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o2) : "r"(sc));
+    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o3) : "r"(sc));
+    *reinterpret_cast<uint4 *>(dst_row + ((i ^ (r & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2_(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int CH>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[CH]);
+template <>
+__device__ __forceinline__ void tmem_ld_n<32>(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld32(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_n<16>(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld16(taddr, r);
+}
+
+struct Fp4Sched {
+  int off[257];  // expert row offsets
+  int tp[257];   // prefix of tiles (or token tiles) per expert
+};
+
+// Prefix over experts of ceil(rows_e / rows_per_tile) * mult, computed by warp 0.
+__device__ __forceinline__ void fp4_prologue(const int32_t *offsets, int E, int rows_per_tile,
+                                             int mult, Fp4Sched &s) {
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s.off[i] = offsets[i];
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int local = 0;
+    for (int e = e0; e < e0 + per && e < E; ++e)
+      local += (s.off[e + 1] - s.off[e] + rows_per_tile - 1) / rows_per_tile * mult;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+      s.tp[e] = run;
+      run += (s.off[e + 1] - s.off[e] + rows_per_tile - 1) / rows_per_tile * mult;
+    }
+    if (lane == 31) s.tp[E] = incl;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ int fp4_find_expert(const Fp4Sched &s, int E, int v) {
+  int lo = 0, hi = E;  // last e with tp[e] <= v
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s.tp[mid] <= v) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+struct Fp4Params {
+  CUtensorMap tmap_act;  // f16 token rows [Tk, K] (x or h), 128-byte swizzle
+  CUtensorMap tmap_q0;   // packed codes [E*N, K/2] of W_gate or W_down
+  CUtensorMap tmap_q1;   // packed codes of W_up (gate/up only)
+  CUtensorMap tmap_s0;   // e4m3 scales [E*N, K/16] of W_gate or W_down
+  CUtensorMap tmap_s1;   // scales of W_up
+  const float *g0;       // global scales [E]: gate or down
+  const float *g1;       // global scales [E]: up
+  const int32_t *offsets;
+  const int32_t *row_src;
+  const float *topk_w;
+  void *out;  // h f16 [Tk, I] or y_partial bf16 [Tk, H]
+  int E, out_cols, w_rows, ksteps, mt;
+  uint32_t *status;
+};
+
+// ---------------------------------------------------------------- weights on M (small batches)
+
+template <int BN_, bool GATEUP>
+struct ExpertGemmFP4 {
+  static constexpr int BN = BN_;
+  static constexpr int NA = GATEUP ? 2 : 1;
+  static constexpr int NW = NA * kTileM;  // weight rows dequantised per stage
+  static constexpr bool CONVERT = true;
+  static constexpr bool F16 = true;
+  static constexpr int RAW_BYTES = NW * kRawRowBytes;
+  static constexpr int TX_BYTES = BN * kTileK * 2 + RAW_BYTES;
+  static constexpr int NBUF = (2 * NA * BN <= 512) ? 2 : 1;
+  static constexpr int STAGE_BYTES = StageGeom<BN, NA, RAW_BYTES>::kBytes;
+  static constexpr int STAGES_FIT = (kSmemLimit - kSmemReserve - (int)sizeof(Fp4Sched)) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+
+  using Params = Fp4Params;
+  using Sched = Fp4Sched;
+  struct Tile {
+    int row0, nrows, arow0, m, e;
+  };
+
+  __device__ static void prologue(const Params &p, Sched &s) { fp4_prologue(p.offsets, p.E, BN, 1, s); }
+  __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E] * p.mt; }
+  __device__ static Tile tile(const Params &p, const Sched &s, int t) {
+    const int tti = t / p.mt, m = t - tti * p.mt;
+    const int e = fp4_find_expert(s, p.E, tti);
+    const int row0 = s.off[e] + (tti - s.tp[e]) * BN;
+    return Tile{row0, min(BN, s.off[e + 1] - row0), e * p.w_rows + m * kTileM, m, e};
+  }
+  __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
+  __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
+    uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
+    tma_load_2d(stage + NA * kATileBytes, &p.tmap_act, bar, k * kTileK, t.row0);
+    tma_load_2d(raw, &p.tmap_q0, bar, k * kPackedRowBytes, t.arow0);
+    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, bar, (k >> 2) * kScaleBoxBytes, t.arow0);
+    if (GATEUP) {
+      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, bar, k * kPackedRowBytes, t.arow0);
+      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, bar,
+                  (k >> 2) * kScaleBoxBytes, t.arow0);
+    }
+  }
+  __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage, int ctid) {
+    const uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
+#pragma unroll
+    for (int i = 0; i < NA; ++i) {
+      const int r = ctid + kTileM * i;
+      const uint32_t sc = *reinterpret_cast<const uint32_t *>(
+          raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4);
+      fp4_row_to_f16(raw + r * kPackedRowBytes, sc, stage + r * 128, r);
+    }
+  }
+  __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
+    constexpr int CH = BN < 32 ? BN : 32;
+    const int f = t.m * kTileM + row;
+    const float ga = __ldg(p.g0 + t.e);
+    const float gb = GATEUP ? __ldg(p.g1 + t.e) : 0.f;
+    for (int c = 0; c < t.nrows; c += CH) {
+      uint32_t a[CH];
+      tmem_ld_n<CH>(taddr + c, a);
+      if (GATEUP) {
+        uint32_t u[CH];
+        tmem_ld_n<CH>(taddr + BN + c, u);
+        tmem_wait_ld();
+        __half *out = static_cast<__half *>(p.out);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+          if (c + j < t.nrows) {
+            const float gv = __uint_as_float(a[j]) * ga;
+            const float hv = gv / (1.0f + __expf(-gv)) * (__uint_as_float(u[j]) * gb);
+            out[(size_t)(t.row0 + c + j) * p.out_cols + f] = __float2half_rn(hv);
+          }
+        }
+      } else {
+        tmem_wait_ld();
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+          if (c + j < t.nrows) {
+            const int r = t.row0 + c + j;
+            const float w = __ldg(p.topk_w + __ldg(p.row_src + r)) * ga;
+            out[(size_t)r * p.out_cols + f] = __float2bfloat16_rn(__uint_as_float(a[j]) * w);
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------- token rows on M (large batches)
+
+template <bool GATEUP>
+struct ExpertGemmTMFP4 {
+  static constexpr int BN = 256;
+  static constexpr int NA = 1;
+  static constexpr int NW = 256;
+  static constexpr bool CONVERT = true;
+  static constexpr bool F16 = true;
+  static constexpr int RAW_BYTES = NW * kRawRowBytes;
+  static constexpr int TX_BYTES = kATileBytes + RAW_BYTES;
+  static constexpr int NBUF = 2;
+  static constexpr int STAGES = 3;
+  static constexpr int FW = GATEUP ? 128 : 256;
+
+  using Params = Fp4Params;
+  using Sched = Fp4Sched;
+  struct Tile {
+    int row0, nrows, brow0, f, e;
+  };
+
+  __device__ static void prologue(const Params &p, Sched &s) {
+    fp4_prologue(p.offsets, p.E, kTileM, p.mt, s);
+  }
+  __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E]; }
+  __device__ static Tile tile(const Params &p, const Sched &s, int t) {
+    const int e = fp4_find_expert(s, p.E, t);
+    const int ntt = (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM;
+    const int local = t - s.tp[e];
+    const int f = local / ntt, tt = local - f * ntt;
+    const int row0 = s.off[e] + tt * kTileM;
+    return Tile{row0, min(kTileM, s.off[e + 1] - row0), e * p.w_rows + f * FW, f, e};
+  }
+  __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
+  __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
+    uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
+    tma_load_2d(stage, &p.tmap_act, bar, k * kTileK, t.row0);
+    tma_load_2d(raw, &p.tmap_q0, bar, k * kPackedRowBytes, t.brow0);
+    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, bar, (k >> 2) * kScaleBoxBytes, t.brow0);
+    if (GATEUP) {
+      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, bar, k * kPackedRowBytes, t.brow0);
+      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, bar,
+                  (k >> 2) * kScaleBoxBytes, t.brow0);
+    }
+  }
+  __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage, int ctid) {
+    const uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
+    uint8_t *b = stage + kATileBytes;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = ctid + kTileM * i;
+      const uint32_t sc = *reinterpret_cast<const uint32_t *>(
+          raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4);
+      fp4_row_to_f16(raw + r * kPackedRowBytes, sc, b + r * 128, r);
+    }
+  }
+  __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
+    const bool valid = row < t.nrows;
+    const float ga = __ldg(p.g0 + t.e);
+    if (GATEUP) {
+      const float gb = __ldg(p.g1 + t.e);
+      __half *dst = static_cast<__half *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + t.f * FW;
+#pragma unroll 1
+      for (int c = 0; c < FW; c += 32) {
+        uint32_t g[32], u[32];
+        tmem_ld32(taddr + c, g);
+        tmem_ld32(taddr + FW + c, u);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = __uint_as_float(g[2 * j]) * ga, g1 = __uint_as_float(g[2 * j + 1]) * ga;
+            const float h0 = g0 / (1.0f + __expf(-g0)) * (__uint_as_float(u[2 * j]) * gb);
+            const float h1 = g1 / (1.0f + __expf(-g1)) * (__uint_as_float(u[2 * j + 1]) * gb);
+            pk[j] = pack_f16x2(h0, h1);
+          }
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    } else {
+      const float w = valid ? __ldg(p.topk_w + __ldg(p.row_src + t.row0 + row)) * ga : 0.f;
+      __nv_bfloat16 *dst =
+          static_cast<__nv_bfloat16 *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + t.f * FW;
+#pragma unroll 1
+      for (int c = 0; c < FW; c += 32) {
+        uint32_t a[32];
+        tmem_ld32(taddr + c, a);
+        tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2_(__uint_as_float(a[2 * j]) * w, __uint_as_float(a[2 * j + 1]) * w);
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------- host side
+
+template <class P>
+moe_status launch_fp4(const Fp4Params &prm, int grid, cudaStream_t stream) {
+  constexpr int smem = smem_bytes_for<P>();
+  static_assert(smem <= kSmemLimit, "shared memory budget");
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  tc_gemm_kernel<P><<<grid, threads_for<P>(), smem, stream>>>(prm);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+bool make_act_map(CUtensorMap *m, const void *base, int K, long rows, int box_rows) {
+  return make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, rows, 64, box_rows, true);
+}
+
+// packed codes [rows, K/2] and scales [rows, K/16] of one weight tensor
+bool make_weight_maps(CUtensorMap *q, CUtensorMap *s, const void *qp, const void *sp, int K,
+                      long rows, int box_rows) {
+  return make_tmap_2d(q, qp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, kPackedRowBytes,
+                      box_rows, false) &&
+         make_tmap_2d(s, sp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, rows, kScaleBoxBytes,
+                      box_rows, false);
+}
+
+Fp4Params base_params(const moe_dims &d, const int32_t *offsets, const int32_t *row_src,
+                      const float *topk_w, uint32_t *status) {
+  Fp4Params prm;
+  prm.offsets = offsets;
+  prm.row_src = row_src;
+  prm.topk_w = topk_w;
+  prm.E = d.E;
+  prm.status = status;
+  return prm;
+}
+
+template <int BN>
+moe_status launch_fp4_small(const moe_dims &d, const moe_experts &ex, const void *x16,
+                            const int32_t *offsets, const int32_t *row_src, const float *topk_w,
+                            void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+  const long Tk = (long)d.T * d.top_k;
+  const long max_tt = Tk / BN + std::min<long>(d.E, Tk);
+  const int sms = device_sm_count();
+  {
+    Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
+    const long rows = (long)d.E * d.I;
+    if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, BN) ||
+        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_gate, ex.s_gate, d.H, rows, kTileM) ||
+        !make_weight_maps(&prm.tmap_q1, &prm.tmap_s1, ex.w_up, ex.s_up, d.H, rows, kTileM))
+      return MOE_ERR_CUDA;
+    prm.g0 = ex.g_gate;
+    prm.g1 = ex.g_up;
+    prm.out = h16;
+    prm.out_cols = d.I;
+    prm.w_rows = d.I;
+    prm.ksteps = d.H / kTileK;
+    prm.mt = d.I / kTileM;
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
+    const moe_status st = launch_fp4<ExpertGemmFP4<BN, true>>(prm, grid, stream);
+    if (st != MOE_OK) return st;
+  }
+  {
+    Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
+    const long rows = (long)d.E * d.H;
+    if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, BN) ||
+        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_down, ex.s_down, d.I, rows, kTileM))
+      return MOE_ERR_CUDA;
+    prm.tmap_q1 = prm.tmap_q0;
+    prm.tmap_s1 = prm.tmap_s0;
+    prm.g0 = ex.g_down;
+    prm.g1 = ex.g_down;
+    prm.out = y_partial;
+    prm.out_cols = d.H;
+    prm.w_rows = d.H;
+    prm.ksteps = d.I / kTileK;
+    prm.mt = d.H / kTileM;
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
+    return launch_fp4<ExpertGemmFP4<BN, false>>(prm, grid, stream);
+  }
+}
+
+moe_status launch_fp4_large(const moe_dims &d, const moe_experts &ex, const void *x16,
+                            const int32_t *offsets, const int32_t *row_src, const float *topk_w,
+                            void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+  const long Tk = (long)d.T * d.top_k;
+  const long max_tt = Tk / kTileM + std::min<long>(d.E, Tk);
+  const int sms = device_sm_count();
+  {
+    using P = ExpertGemmTMFP4<true>;
+    Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
+    const long rows = (long)d.E * d.I;
+    if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, kTileM) ||
+        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_gate, ex.s_gate, d.H, rows, 128) ||
+        !make_weight_maps(&prm.tmap_q1, &prm.tmap_s1, ex.w_up, ex.s_up, d.H, rows, 128))
+      return MOE_ERR_CUDA;
+    prm.g0 = ex.g_gate;
+    prm.g1 = ex.g_up;
+    prm.out = h16;
+    prm.out_cols = d.I;
+    prm.w_rows = d.I;
+    prm.ksteps = d.H / kTileK;
+    prm.mt = d.I / P::FW;
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
+    const moe_status st = launch_fp4<P>(prm, grid, stream);
+    if (st != MOE_OK) return st;
+  }
+  {
+    using P = ExpertGemmTMFP4<false>;
+    Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
+    const long rows = (long)d.E * d.H;
+    if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, kTileM) ||
+        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_down, ex.s_down, d.I, rows, 256))
+      return MOE_ERR_CUDA;
+    prm.tmap_q1 = prm.tmap_q0;
+    prm.tmap_s1 = prm.tmap_s0;
+    prm.g0 = ex.g_down;
+    prm.g1 = ex.g_down;
+    prm.out = y_partial;
+    prm.out_cols = d.H;
+    prm.w_rows = d.H;
+    prm.ksteps = d.I / kTileK;
+    prm.mt = d.H / P::FW;
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
+    return launch_fp4<P>(prm, grid, stream);
+  }
+}
+
+__global__ void bf16_to_f16_kernel(const __nv_bfloat162 *__restrict__ in, __half2 *__restrict__ out,
+                                   size_t n2) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n2;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = __float22half2_rn(__bfloat1622float2(in[i]));
+}
+
+}  // namespace
+
+moe_status launch_bf16_to_f16(const void *in, void *out, size_t n, cudaStream_t stream) {
+  const size_t n2 = n / 2;
+  if (n2 == 0) return MOE_OK;
+  const int blocks = (int)std::min<size_t>((n2 + 255) / 256, (size_t)device_sm_count() * 16);
+  bf16_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat162 *>(in),
+                                                 static_cast<__half2 *>(out), n2);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const void *x16,
+                              const int32_t *expert_offsets, const int32_t *row_src,
+                              const float *topk_w, void *y_partial, void *h16, uint32_t *status,
+                              cudaStream_t stream) {
+  const long mean_rows = ((long)d.T * d.top_k + d.E - 1) / d.E;
+  if (mean_rows >= 128 && d.H % 256 == 0)
+    return launch_fp4_large(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status,
+                            stream);
+  switch (expert_bn(d)) {
+    case 16: return launch_fp4_small<16>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 32: return launch_fp4_small<32>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 64: return launch_fp4_small<64>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 128: return launch_fp4_small<128>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
+    default: return launch_fp4_small<256>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
+  }
+}
+
+}  // namespace beam

@@ -59,11 +59,12 @@ struct WsLayout {
   size_t counts = 0, bases = 0;                     // permute
   size_t offsets = 0, slot_of = 0, row_src = 0, x_perm = 0;  // forward only
   size_t h = 0;                                     // experts
+  size_t x16 = 0;                                   // experts, NVFP4 only
   size_t y_partial = 0;                             // forward only
   size_t total = 0;
 };
 
-inline WsLayout ws_layout(const moe_dims &d, moe_op op) {
+inline WsLayout ws_layout(const moe_dims &d, moe_op op, moe_wdtype wdtype = MOE_W_BF16) {
   WsLayout L;
   size_t off = kHeaderBytes;
   auto take = [&](size_t bytes) {
@@ -94,6 +95,7 @@ inline WsLayout ws_layout(const moe_dims &d, moe_op op) {
     L.x_perm = take(Tk * d.H * 2);
   }
   if (op == MOE_OP_EXPERTS || fwd) L.h = take(Tk * d.I * 2);
+  if (op == MOE_OP_EXPERTS && wdtype == MOE_W_NVFP4) L.x16 = take(Tk * d.H * 2);
   if (fwd) L.y_partial = take(Tk * d.H * 2);
   L.total = off;
   return L;
@@ -106,6 +108,12 @@ inline WsLayout ws_layout(const moe_dims &d, moe_op op) {
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                        uint32_t box_outer);
 
+// Any 2-D tensor [outer, inner] with a {box_inner, box_outer} box; 128-byte
+// swizzle or none; zero fill out of bounds.
+bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                  bool swizzle128);
+
 int device_sm_count();
 
 // ------------------------------------------------------------------ launchers
@@ -116,12 +124,22 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
 
 moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
                           int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
-                          int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream);
+                          int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream,
+                          bool f16_out = false);
 
 moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *x_perm,
                           const int32_t *expert_offsets, const int32_t *row_src,
                           const float *topk_w, void *y_partial, __nv_bfloat16 *h,
                           uint32_t *status, cudaStream_t stream);
+
+// NVFP4 expert weights: x16 and h16 are f16 [Tk, H] and [Tk, I].
+moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const void *x16,
+                              const int32_t *expert_offsets, const int32_t *row_src,
+                              const float *topk_w, void *y_partial, void *h16, uint32_t *status,
+                              cudaStream_t stream);
+
+// n bf16 values -> f16 (n even).
+moe_status launch_bf16_to_f16(const void *in, void *out, size_t n, cudaStream_t stream);
 
 moe_status launch_combine(const moe_dims &d, const void *y_partial, const int32_t *slot_of, void *y,
                           cudaStream_t stream);

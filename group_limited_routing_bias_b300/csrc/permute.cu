@@ -8,6 +8,8 @@
 //   permute_scan_kernel    one CTA: per-chunk bases and expert offsets
 //   permute_scatter_kernel one CTA per chunk: warp-ordered ranks -> slots
 //   permute_gather_kernel  all SMs: copy x rows into x_perm (16-byte vectors)
+#include <cuda_fp16.h>
+
 #include "moe_internal.cuh"
 
 namespace beam {
@@ -132,6 +134,9 @@ __global__ void __launch_bounds__(kChunkThreads)
   }
 }
 
+// Copies x rows into permuted order; with TO_F16 the bf16 values are written
+// as f16 (exact for |v| >= 2^-14; the NVFP4 expert GEMMs run on f16 operands).
+template <bool TO_F16>
 __global__ void __launch_bounds__(256)
     permute_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ row_src,
                           const int32_t *__restrict__ offsets, int E, int top_k, int vec_per_row,
@@ -143,7 +148,19 @@ __global__ void __launch_bounds__(256)
     const int t = row_src[r] / top_k;
     const uint4 *src = x + (size_t)t * vec_per_row;
     uint4 *dst = x_perm + (size_t)r * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
+    for (int v = lane; v < vec_per_row; v += 32) {
+      uint4 q = src[v];
+      if (TO_F16) {
+        uint32_t *w = reinterpret_cast<uint32_t *>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+          const __half2 h = __float22half2_rn(f);
+          w[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+      }
+      dst[v] = q;
+    }
   }
 }
 
@@ -151,7 +168,8 @@ __global__ void __launch_bounds__(256)
 
 moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
                           int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
-                          int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream) {
+                          int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream,
+                          bool f16_out) {
   const int Tk = d.T * d.top_k;
   const int nchunks = std::max(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
   static bool attr_set = false;
@@ -169,9 +187,14 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
                                                                           slot_of, row_src);
   if (Tk > 0) {
     const int blocks = std::max(1, std::min((Tk + 7) / 8, device_sm_count() * 8));
-    permute_gather_kernel<<<blocks, 256, 0, stream>>>(
-        static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
-        static_cast<uint4 *>(x_perm));
+    if (f16_out)
+      permute_gather_kernel<true><<<blocks, 256, 0, stream>>>(
+          static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
+          static_cast<uint4 *>(x_perm));
+    else
+      permute_gather_kernel<false><<<blocks, 256, 0, stream>>>(
+          static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
+          static_cast<uint4 *>(x_perm));
   }
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -150,6 +150,13 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// Same with f16 A and B.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | ((uint32_t)(N >> 3) << 17)   // N / 8   (A, B format 0: f16)
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(

@@ -56,6 +56,11 @@ struct RouterLogits {
   struct Tile {
     int m0, kbeg, kend, split;
   };
+  static constexpr bool CONVERT = false;
+  static constexpr bool F16 = false;
+  static constexpr int RAW_BYTES = 0;
+  static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
+  __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
   __device__ static void prologue(const Params &, Sched &) {}
   __device__ static int num_tiles(const Params &, const Sched &) { return gridDim.x; }
   __device__ static Tile tile(const Params &p, const Sched &, int t) {

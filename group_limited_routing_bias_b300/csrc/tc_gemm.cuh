@@ -11,8 +11,14 @@
 // The accumulators are double-buffered in tensor memory when they fit, so
 // the epilogue of one tile overlaps the main loop of the next.
 //
+// Problems whose weights arrive packed (NVFP4) add a converter role:
+//   warps 8..11   : wait for a stage's raw bytes, dequantise them into the
+//                   stage's swizzled operand tile, fence the generic proxy
+//                   against the tensor cores' async proxy, then signal the MMA.
+//
 // A problem class P supplies the shapes and the tile schedule:
-//   static constexpr int BN, NA, STAGES, NBUF;
+//   static constexpr int BN, NA, STAGES, NBUF, RAW_BYTES, TX_BYTES;
+//   static constexpr bool CONVERT, F16;   (packed weights; f16 instead of bf16 operands)
 //   struct Params { ...; uint32_t *status; };  struct Sched;  struct Tile;
 //   static void prologue(const Params&, Sched&)   (all threads; may __syncthreads)
 //   static int  num_tiles(const Params&, const Sched&)
@@ -20,6 +26,7 @@
 //   static int  num_k(const Params&, const Tile&)
 //   static void load(const Params&, const Tile&, int k, uint8_t *stage, uint64_t *bar)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
+//   static void convert(const Params&, const Tile&, int k, uint8_t *stage, int ctid)  (CONVERT)
 #pragma once
 
 #include "ptx.cuh"
@@ -32,23 +39,39 @@ constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;                // 227 KB dynamic shared memory
 constexpr int kSmemReserve = 4096;                // alignment slack + barriers
 
-template <int BN, int NA>
+template <int BN, int NA, int RAW = 0>
 struct StageGeom {
-  static constexpr int kBytes = NA * kATileBytes + BN * kTileK * 2;
+  static constexpr int kOperandBytes = NA * kATileBytes + BN * kTileK * 2;
+  static constexpr int kBytes = kOperandBytes + RAW;
   static_assert(kBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
 
 template <class P>
-constexpr int smem_bytes_for() {
-  return kSmemReserve + P::STAGES * StageGeom<P::BN, P::NA>::kBytes + (int)sizeof(typename P::Sched);
+__host__ __device__ constexpr int stage_bytes_of() {
+  return StageGeom<P::BN, P::NA, P::RAW_BYTES>::kBytes;
 }
 
 template <class P>
-__global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__ typename P::Params p) {
-  constexpr int STAGE = StageGeom<P::BN, P::NA>::kBytes;
+__host__ __device__ constexpr int smem_bytes_for() {
+  return kSmemReserve + P::STAGES * stage_bytes_of<P>() + (int)sizeof(typename P::Sched);
+}
+
+template <class P>
+__host__ __device__ constexpr int threads_for() {
+  return P::CONVERT ? 384 : 256;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <class P>
+__global__ void __launch_bounds__(threads_for<P>(), 1)
+    tc_gemm_kernel(const __grid_constant__ typename P::Params p) {
+  constexpr int STAGE = stage_bytes_of<P>();
   constexpr uint32_t kAccCols = P::NA * P::BN;
   constexpr uint32_t kTmemCols = tmem_cols_pow2(P::NBUF * kAccCols);
-  constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, P::BN);
+  constexpr uint32_t kIdesc = P::F16 ? umma_idesc_f16(kTileM, P::BN) : umma_idesc_bf16(kTileM, P::BN);
   static_assert(P::NBUF * kAccCols <= 512, "accumulators exceed tensor memory");
   static_assert(P::BN % 16 == 0 && P::BN >= 16 && P::BN <= 256, "invalid MMA N");
 
@@ -59,7 +82,8 @@ __global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__
   uint64_t *empty = full + P::STAGES;
   uint64_t *tfull = empty + P::STAGES;
   uint64_t *tempty = tfull + P::NBUF;
-  uint64_t *drain = tempty + P::NBUF;
+  uint64_t *ready = tempty + P::NBUF;  // converters -> MMA (CONVERT only)
+  uint64_t *drain = ready + P::STAGES;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   typename P::Sched *sched =
@@ -77,6 +101,7 @@ __global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
+    for (int s = 0; s < P::STAGES; ++s) mbar_init(&ready[s], 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -106,7 +131,7 @@ __global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE);
+          mbar_arrive_expect_tx(&full[stage], P::TX_BYTES);
           P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
           issued |= 1u << stage;
           par = (par & ~(1u << stage)) | (ph << stage);
@@ -137,7 +162,7 @@ __global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__
         tc_fence_after();
         const uint32_t d0 = tmem_base + buf * kAccCols;
         for (int k = 0; k < nk; ++k) {
-          if (!mbar_wait(&full[stage], ph, abort_flag, p.status)) {
+          if (!mbar_wait(P::CONVERT ? &ready[stage] : &full[stage], ph, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -172,7 +197,33 @@ __global__ void __launch_bounds__(256, 1) tc_gemm_kernel(const __grid_constant__
         mbar_drain_wait(drain, 0);
       }
     }
-  } else if (warp >= 4) {
+  } else if (P::CONVERT && warp >= 8) {
+    // ---------------- converters: raw packed weights -> swizzled operand tile
+    const int ctid = threadIdx.x - 256;
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const typename P::Tile tile = P::tile(p, *sched, t);
+      const int nk = P::num_k(p, tile);
+      for (int k = 0; k < nk; ++k) {
+        bool got = mbar_wait(&full[stage], ph, abort_flag, p.status);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        P::convert(p, tile, k, stages + stage * STAGE, ctid);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[stage]);
+        if (++stage == P::STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;

@@ -177,7 +177,20 @@ typedef struct {
   const void *data;
   const uint8_t *scales;
   double global;
+  double e2m1[16];  /* value of every e2m1 code (NVFP4 only) */
+  double e4m3[256]; /* value of every e4m3 code (NVFP4 only) */
 } oracle_matrix;
+
+static oracle_matrix make_matrix(int dtype, const void *data, const uint8_t *scales, double global) {
+  oracle_matrix m;
+  m.dtype = dtype;
+  m.data = data;
+  m.scales = scales;
+  m.global = global;
+  for (int c = 0; c < 16; ++c) m.e2m1[c] = oracle_e2m1_value((uint8_t)c);
+  for (int c = 0; c < 256; ++c) m.e4m3[c] = oracle_e4m3_value((uint8_t)c);
+  return m;
+}
 
 static void decode_row(const oracle_matrix *m, int K, int row, double *out) {
   if (m->dtype == 0) {
@@ -189,7 +202,7 @@ static void decode_row(const oracle_matrix *m, int K, int row, double *out) {
     for (int k = 0; k < K; ++k) {
       uint8_t byte = q[k / 2];
       uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
-      out[k] = oracle_e2m1_value(code) * oracle_e4m3_value(sc[k / 16]) * m->global;
+      out[k] = m->e2m1[code] * m->e4m3[sc[k / 16]] * m->global;
     }
   }
 }
@@ -198,7 +211,7 @@ static void decode_row(const oracle_matrix *m, int K, int row, double *out) {
 int oracle_decode_matrix(int dtype, int N, int K, const void *data,
                          const uint8_t *scales, double global, double *out) {
   if (N <= 0 || K <= 0 || (dtype == 1 && K % 16 != 0)) return ORACLE_BAD_ARG;
-  oracle_matrix m = {dtype, data, scales, global};
+  oracle_matrix m = make_matrix(dtype, data, scales, global);
 #pragma omp parallel for schedule(static)
   for (int n = 0; n < N; ++n) decode_row(&m, K, n, out + (size_t)n * K);
   return ORACLE_OK;
@@ -219,7 +232,8 @@ int oracle_expert_swiglu(int n, int H, int I, const uint16_t *x,
                          double *o) {
   if (n < 0 || H <= 0 || I <= 0) return ORACLE_BAD_ARG;
   if (n == 0) return ORACLE_OK;
-  oracle_matrix mg = {dtype, wg, sg, gg}, mu = {dtype, wu, su, gu}, md = {dtype, wd, sd, gd};
+  oracle_matrix mg = make_matrix(dtype, wg, sg, gg), mu = make_matrix(dtype, wu, su, gu),
+                md = make_matrix(dtype, wd, sd, gd);
   double *xd = (double *)malloc(sizeof(double) * (size_t)n * H);
   double *act = (double *)malloc(sizeof(double) * (size_t)n * I);
   if (!xd || !act) { free(xd); free(act); return ORACLE_BAD_ARG; }

@@ -5,12 +5,16 @@ Rule for routing: expert indices must match the oracle exactly, except for
 tokens where the oracle's decision is a near tie: the gap between the
 kept/dropped groups (topk_group-th vs next group score) or between any two
 neighbours among the top_k + 1 best candidate biased scores is below 1e-5.
-Such tokens are counted; the GPU's choice is accepted for them when its total
-biased score is within top_k * 1e-5 of the oracle's, and their reference
-output is then computed with the GPU's indices (weights from the oracle's
-unbiased scores).
+Such tokens are counted.  For each, the GPU's answer must still be valid: it
+must equal, position by position within 1e-5 of biased score, the top_k of one
+of the kept-group sets that the near ties allow (groups scoring above the
+boundary are kept; among those within 1e-5 of it, every choice of the
+remaining count is tried).  The reference output of such a token is then
+computed with the GPU's indices (weights from the oracle's unbiased scores).
 """
 from __future__ import annotations
+
+import itertools
 
 from dataclasses import dataclass, field
 
@@ -38,6 +42,7 @@ class RoutingReport:
     mismatched: int                      # unflagged tokens whose indices differ
     weight_max_rel: float
     use_gpu: np.ndarray = field(repr=False)  # bool [T]: reference uses the GPU's indices
+    mismatch_info: list = field(default_factory=list)  # details of up to 4 mismatched tokens
 
     @property
     def ok(self) -> bool:
@@ -58,6 +63,41 @@ def near_tie_mask(orc, n_group, topk_group, top_k, eps=TIE_EPS) -> np.ndarray:
     return np.minimum(group_gap, gaps.min(axis=1)) < eps
 
 
+def allowed_selections(orc, t, n_group, topk_group, top_k, eps=TIE_EPS):
+    """Every top_k selection (experts ordered by biased score, then index) that
+    some eps-perturbation of the oracle's group scores could produce."""
+    E = orc.biased.shape[1]
+    gsz = E // n_group
+    gs = orc.group_score[t].astype(np.float64)
+    order = sorted(range(n_group), key=lambda j: (-gs[j], j))
+    thr = gs[order[topk_group - 1]]
+    forced = [j for j in range(n_group) if gs[j] > thr + eps]
+    tie = [j for j in range(n_group) if abs(gs[j] - thr) <= eps]
+    sb = orc.biased[t].astype(np.float64)
+    out = []
+    for extra in itertools.combinations(tie, topk_group - len(forced)):
+        kept = set(forced) | set(extra)
+        cand = [e for e in range(E) if e // gsz in kept]
+        out.append((kept, sorted(cand, key=lambda e: (-sb[e], e))[:top_k]))
+    return out
+
+
+def gpu_choice_valid(orc, t, g, n_group, topk_group, top_k, eps=TIE_EPS) -> bool:
+    E = orc.biased.shape[1]
+    gsz = E // n_group
+    g = [int(e) for e in g]
+    if len(set(g)) != top_k or any(e < 0 or e >= E for e in g):
+        return False
+    sb = orc.biased[t].astype(np.float64)
+    if any(sb[g[i]] < sb[g[i + 1]] - eps for i in range(top_k - 1)):
+        return False  # not in descending order
+    for kept, sel in allowed_selections(orc, t, n_group, topk_group, top_k, eps):
+        if all(e // gsz in kept for e in g) and \
+                all(abs(sb[a] - sb[b]) <= eps for a, b in zip(g, sel)):
+            return True
+    return False
+
+
 def compare_routing(orc, gpu_idx, gpu_w, n_group, topk_group, top_k, routed_scale) -> RoutingReport:
     gpu_idx = np.asarray(gpu_idx)
     gpu_w = np.asarray(gpu_w)
@@ -66,16 +106,25 @@ def compare_routing(orc, gpu_idx, gpu_w, n_group, topk_group, top_k, routed_scal
     same = np.all(gpu_idx == orc.idx, axis=1)
     mismatched = int(np.sum(~same & ~flagged))
     use_gpu = ~same & flagged
-    for t in np.nonzero(use_gpu)[0]:
+    info = []
+
+    def describe(t):
         g = gpu_idx[t]
-        ok = len(set(g.tolist())) == top_k and np.all((g >= 0) & (g < E))
-        if ok:
-            obj_gpu = orc.biased[t, g].astype(np.float64).sum()
-            obj_orc = orc.biased[t, orc.idx[t]].astype(np.float64).sum()
-            ok = abs(obj_gpu - obj_orc) <= top_k * TIE_EPS
-        if not ok:
+        valid = np.all((g >= 0) & (g < E))
+        gs = np.sort(orc.group_score[t].astype(np.float64))[::-1]
+        return dict(t=int(t), flagged=bool(flagged[t]), oracle=orc.idx[t].tolist(), gpu=g.tolist(),
+                    oracle_biased=orc.biased[t, orc.idx[t]].tolist(),
+                    gpu_biased=orc.biased[t, g].tolist() if valid else None,
+                    group_scores_sorted=gs.tolist())
+
+    for t in np.nonzero(~same & ~flagged)[0][:4]:
+        info.append(describe(t))
+    for t in np.nonzero(use_gpu)[0]:
+        if not gpu_choice_valid(orc, t, gpu_idx[t], n_group, topk_group, top_k):
             mismatched += 1
             use_gpu[t] = False
+            if len(info) < 4:
+                info.append(describe(t))
     # weights: against the oracle's unbiased scores for whichever indices are used
     ref_w = orc.w.astype(np.float64).copy()
     for t in np.nonzero(use_gpu)[0]:
@@ -84,7 +133,7 @@ def compare_routing(orc, gpu_idx, gpu_w, n_group, topk_group, top_k, routed_scal
     good = same | use_gpu
     rel = np.abs(gpu_w.astype(np.float64) - ref_w) / np.abs(ref_w)
     wmax = float(rel[good].max()) if good.any() else 0.0
-    return RoutingReport(T, int(flagged.sum()), int(use_gpu.sum()), mismatched, wmax, use_gpu)
+    return RoutingReport(T, int(flagged.sum()), int(use_gpu.sum()), mismatched, wmax, use_gpu, info)
 
 
 def reference_routing(orc, report: RoutingReport, gpu_idx, routed_scale):

@@ -1,0 +1,140 @@
+"""GPU parity with NVFP4 expert weights (e2m1 codes, one e4m3 scale per 16 k,
+one fp32 global per expert and matrix), through the C ABI, against the oracle
+evaluated on the same packed bytes.
+
+The GPU dequantises exactly (code * scale is exact in f16; the global scale
+multiplies the fp32 accumulator), so the output error is the 16-bit rounding
+of h and y_partial, as with bf16 weights: the tests hold it to the bf16 bars
+(max|err| <= 2e-2 max|ref|, relative Frobenius <= 5e-3), tighter than the
+3e-2 relative Frobenius allowed for this workload.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from parity import NVFP4_REL_FROB, compare_routing, output_errors, reference_routing
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+TINY4 = mi.MoeConfig("tiny-nvfp4", T=64, H=256, E=32, n_group=8, topk_group=2, top_k=4, I=256,
+                     weights="nvfp4")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import group_limited_routing_bias_b300 as m
+    return m
+
+
+class Fp4Case:
+    def __init__(self, cfg, T=None, seed=0):
+        self.cfg = cfg if T is None else cfg.with_T(T)
+        c = self.cfg
+        x, wr, b = mi.make_router_inputs(c, seed=seed)
+        self.x_h, self.wr_h, self.b_h = x, wr, b
+        self.x, self.wr, self.b = x.to(DEV), wr.to(DEV), b.to(DEV)
+        packed = []
+        for w in mi.make_expert_weights(c, device=DEV, seed=seed):
+            packed.append(mi.quantize_experts_nvfp4(w))
+            del w
+        (self.qg, self.sg, self.gg), (self.qu, self.su, self.gu), (self.qd, self.sd, self.gd) = packed
+        torch.cuda.empty_cache()
+
+    def experts(self, lib):
+        return lib.Experts(self.qg, self.qu, self.qd, self.sg, self.su, self.sd, self.gg, self.gu,
+                           self.gd)
+
+    def get_expert(self, e):
+        M = oracle.Nvfp4Matrix
+        return (M(self.qg[e].cpu().numpy(), self.sg[e].cpu().numpy(), float(self.gg[e])),
+                M(self.qu[e].cpu().numpy(), self.su[e].cpu().numpy(), float(self.gu[e])),
+                M(self.qd[e].cpu().numpy(), self.sd[e].cpu().numpy(), float(self.gd[e])))
+
+
+def forward(lib, case):
+    c = case.cfg
+    d = lib.dims_of(c)
+    ws = lib.alloc_workspace(d, lib.MOE_OP_FORWARD, lib.MOE_W_NVFP4)
+    y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(c.T, c.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(c.T, c.top_k, dtype=torch.float32, device=DEV)
+    lib.moe_forward(d, case.x, case.wr, case.b, case.experts(lib), y, ws, idx, w)
+    assert lib.workspace_status(ws) == 0
+    return y, idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check(lib, case, sample=None):
+    c = case.cfg
+    y, idx, w = forward(lib, case)
+    orc = oracle.route(mi.bf16_bits(case.x_h), case.wr_h.numpy(), case.b_h.numpy(), c.n_group,
+                       c.topk_group, c.top_k, c.routed_scale, details=True)
+    rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
+    assert rep.ok, (rep, rep.mismatch_info)
+    ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
+    tokens = np.arange(c.T) if sample is None else np.asarray(sample)
+    y_ref = oracle.experts_forward(mi.bf16_bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
+    err = output_errors(y.double().cpu().numpy()[tokens], y_ref)
+    print(f"\n[{c.name} T={c.T}] routing {rep}; output {err} over {len(tokens)} tokens")
+    assert err.rel_frob <= NVFP4_REL_FROB
+    assert err.ok(), err
+    return y
+
+
+@pytest.mark.parametrize("T", [64, 200, 1, 2048])
+def test_nvfp4_tiny(lib, T):
+    """T=2048 gives 256 rows per expert: the token-major NVFP4 GEMMs."""
+    check(lib, Fp4Case(TINY4, T=T))
+
+
+@pytest.mark.parametrize("T,n_sample", [(1, None), (64, None), (1024, 64), (16384, 48)])
+def test_nvfp4_beam(lib, T, n_sample):
+    case = Fp4Case(mi.CONFIGS["nvfp4"], T=T)
+    sample = None
+    if n_sample is not None:
+        sample = np.sort(np.random.default_rng(T).choice(T, n_sample, replace=False))
+    check(lib, case, sample)
+
+
+def test_nvfp4_experts_entry_point_matches_forward(lib):
+    """moe_experts_swiglu with NVFP4 weights (bf16 x_perm converted inside)
+    gives the same y as moe_forward, bit for bit."""
+    c = TINY4.with_T(300)
+    case = Fp4Case(c)
+    d = lib.dims_of(c)
+    y_fwd, _, _ = forward(lib, case)
+    Tk = c.T * c.top_k
+    idx = torch.empty(c.T, c.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(c.T, c.top_k, dtype=torch.float32, device=DEV)
+    lib.moe_route(d, case.x, case.wr, case.b, idx, w, lib.alloc_workspace(d, lib.MOE_OP_ROUTE))
+    x_perm = torch.empty(Tk, c.H, dtype=torch.bfloat16, device=DEV)
+    offs = torch.empty(c.E + 1, dtype=torch.int32, device=DEV)
+    slot_of = torch.empty(Tk, dtype=torch.int32, device=DEV)
+    row_src = torch.empty(Tk, dtype=torch.int32, device=DEV)
+    lib.moe_permute(d, idx, case.x, x_perm, offs, slot_of, row_src,
+                    lib.alloc_workspace(d, lib.MOE_OP_PERMUTE))
+    y_partial = torch.empty(Tk, c.H, dtype=torch.bfloat16, device=DEV)
+    ws = lib.alloc_workspace(d, lib.MOE_OP_EXPERTS, lib.MOE_W_NVFP4)
+    lib.moe_experts_swiglu(d, case.experts(lib), x_perm, offs, row_src, w, y_partial, ws)
+    y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=DEV)
+    lib.moe_combine(d, y_partial, slot_of, y)
+    assert lib.workspace_status(ws) == 0
+    assert torch.equal(y, y_fwd)
+
+
+def test_nvfp4_rejects_unsupported_shape(lib):
+    """NVFP4 needs H and I multiples of 256 (a scale box spans 256 k)."""
+    c = mi.CONFIGS["tiny"]  # I = 128
+    case = Fp4Case(TINY4)
+    d = lib.dims_of(c)
+    ws = lib.alloc_workspace(d, lib.MOE_OP_FORWARD, lib.MOE_W_NVFP4)
+    y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=DEV)
+    ex = lib.Experts(case.qg[:, :128].contiguous(), case.qu[:, :128].contiguous(),
+                     case.qd[:, :, :64].contiguous(), case.sg[:, :128].contiguous(),
+                     case.su[:, :128].contiguous(), case.sd[:, :, :8].contiguous(), case.gg, case.gu,
+                     case.gd)
+    with pytest.raises(lib.MoeError) as e:
+        lib.moe_forward(d, case.x, case.wr, case.b, ex, y, ws)
+    assert e.value.status == 2

@@ -68,7 +68,7 @@ def check_routing(case, orc, idx, w, max_flag_frac=0.05):
     c = case.cfg
     rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
     print(f"\n[{c.name} T={c.T}] routing: {rep}")
-    assert rep.ok, rep
+    assert rep.ok, (rep, rep.mismatch_info)
     assert rep.flagged <= max(2, max_flag_frac * c.T)
     return rep
 
