@@ -42,6 +42,19 @@ FLOP_PER_TOKEN = 2 * 3 * 5120 * 2560 * 8  # expert FLOPs per token (8 routed exp
 L2_FLUSH_BYTES = 512 << 20
 
 
+def traffic_per_touched_expert():
+    """DRAM bytes per touched expert of the decode expert GEMMs, from the committed
+    ncu figure (small-case capture, scaled by touched experts)."""
+    p = os.path.join(ROOT, "profiles", "expert_gemms_decode_traffic.md")
+    try:
+        for line in open(p):
+            if line.startswith("bytes_per_touched_expert:"):
+                return int(line.split(":")[1])
+    except OSError:
+        pass
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -113,7 +126,8 @@ class Workload:
         self.x_host = x.pin_memory()
         self.x, self.wr, self.b = x.to(dev), wr.to(dev), b.to(dev)
         self.experts = lib.Experts(*weights)
-        self.ws = lib.alloc_workspace(self.d, lib.MOE_OP_FORWARD, device=dev)
+        self.wdtype = self.experts.dtype
+        self.ws = lib.alloc_workspace(self.d, lib.MOE_OP_FORWARD, self.wdtype, device=dev)
         T, H, k, E = cfg.T, cfg.H, cfg.top_k, cfg.E
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
         self.idx = torch.empty(T, k, dtype=torch.int32, device=dev)
@@ -129,7 +143,7 @@ class Workload:
         self.y_partial = torch.empty(Tk, H, dtype=torch.bfloat16, device=dev)
         self.ws_route = lib.alloc_workspace(self.d, lib.MOE_OP_ROUTE, device=dev)
         self.ws_perm = lib.alloc_workspace(self.d, lib.MOE_OP_PERMUTE, device=dev)
-        self.ws_exp = lib.alloc_workspace(self.d, lib.MOE_OP_EXPERTS, device=dev)
+        self.ws_exp = lib.alloc_workspace(self.d, lib.MOE_OP_EXPERTS, self.wdtype, device=dev)
 
     def forward(self, lib):
         lib.moe_forward(self.d, self.x, self.wr, self.b, self.experts, self.y, self.ws, self.idx,
@@ -182,6 +196,68 @@ def e2e_steps(lib, wl, steps, flush):
         wl.forward(lib)
         wl.y_host.copy_(wl.y, non_blocking=True)
     return time_steps(step, steps, flush)
+
+
+FP4_EXPERT_BYTES = 3 * (5120 * 2560 // 2 + 5120 * 2560 // 16) + 3 * 4  # codes + e4m3 scales + globals
+
+
+def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
+    """Prefill (T=16384) as a secondary figure, with clocks sampled over its timed
+    steps: sustained tensor work runs power-capped, so the peak it is compared
+    with is the sustained one when the clocks sat below max, else the burst one."""
+    pw = Workload(lib, cfg, weights, dev)
+    for _ in range(2):
+        pw.forward(lib)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    p_ms = statistics.mean(time_steps(lambda: pw.forward(lib), steps, flush))
+    p_stage = stage_breakdown(lib, pw, 3, flush)
+    clocks = sampler.stop()
+    assert lib.workspace_status(pw.ws) == 0
+    flop = cfg.T * FLOP_PER_TOKEN
+    tflops = flop / (p_stage["experts"] / 1000.0) / 1e12
+    capped = bool(clocks["sm_mhz"] and clocks["sm_max_mhz"] and
+                  clocks["sm_mhz"] < 0.9 * clocks["sm_max_mhz"])
+    peak = peaks["bf16_sust"] if capped else peaks["bf16"]
+    out = {"workload": f"{cfg.name} T={cfg.T}", "tokens_per_s": cfg.T / (p_ms / 1000.0),
+           "ms_per_step": p_ms, "stages_ms": p_stage, "expert_gemm_tflops": tflops,
+           "layer_tflops": flop / (p_ms / 1000.0) / 1e12,
+           "peak_bf16_tflops": peak, "peak_kind": "sustained" if capped else "burst",
+           "frac_of_bf16_peak": tflops / peak,
+           "frac_of_burst_peak": tflops / peaks["bf16"], "clocks": clocks}
+    del pw
+    torch.cuda.empty_cache()
+    return out
+
+
+def nvfp4_figures(lib, mi, fp4w, dev, flush, peaks, args):
+    """NVFP4 experts: decode T=64 (HBM-bound: packed bytes of touched experts) and
+    prefill T=16384 (W4A16: the bf16 tensor peak is its denominator)."""
+    out = {}
+    for name, T, steps in (("decode", 64, 50), ("prefill", 16384, 5)):
+        cfg = mi.CONFIGS["nvfp4"].with_T(T)
+        wl = Workload(lib, cfg, fp4w, dev)
+        for _ in range(3):
+            wl.forward(lib)
+        torch.cuda.synchronize()
+        ms = statistics.mean(time_steps(lambda: wl.forward(lib), steps, flush))
+        st = stage_breakdown(lib, wl, min(steps, 20), flush)
+        assert lib.workspace_status(wl.ws) == 0 and lib.workspace_status(wl.ws_exp) == 0
+        touched = int(len(np.unique(wl.idx.cpu().numpy())))
+        fig = {"T": T, "tokens_per_s": T / (ms / 1000.0), "ms_per_step": ms, "stages_ms": st,
+               "touched_experts": touched}
+        if name == "decode":
+            gbs = touched * FP4_EXPERT_BYTES / (st["experts"] / 1000.0) / 1e9
+            fig.update({"expert_gemm_gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm"],
+                        "frac_of_8tbs_nominal": gbs / 8000.0})
+        else:
+            tf = T * FLOP_PER_TOKEN / (st["experts"] / 1000.0) / 1e12
+            fig.update({"expert_gemm_tflops": tf, "frac_of_bf16_burst_peak": tf / peaks["bf16"]})
+        out[name] = fig
+        del wl
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -310,6 +386,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-nvfp4", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--profile", choices=["decode", "prefill", "skewed", "prefill-small",
                                           "decode-small"], default=None,
@@ -386,7 +463,8 @@ def main():
     exp_bytes = touched * EXPERT_BYTES + act_bytes
     achieved = exp_bytes / (stages["experts"] / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm"], "traffic": None,
+                "frac": achieved / peaks["hbm"],
+                "traffic": (tpe * touched if (tpe := traffic_per_touched_expert()) else None),
                 "kernel": "expert GEMMs (gate/up + SwiGLU, down + routing weight): one "
                           "moe_experts_swiglu call, two launches",
                 "peak_source": peaks["src"], "frac_of_8tbs_nominal": achieved / 8000.0,
@@ -401,22 +479,17 @@ def main():
     # ---- prefill, secondary figure (same weights: identical shapes and seeds)
     prefill = None
     if not args.no_prefill:
-        pcfg = mi.CONFIGS["prefill"]
         del wl.x_perm, wl.y_partial
-        pw = Workload(lib, pcfg, weights, dev)
-        for _ in range(2):
-            pw.forward(lib)
-        torch.cuda.synchronize()
-        p_ms = statistics.mean(time_steps(lambda: pw.forward(lib), args.prefill_steps, flush))
-        p_stage = stage_breakdown(lib, pw, 3, flush)
-        tflops = pcfg.T * FLOP_PER_TOKEN / (p_stage["experts"] / 1000.0) / 1e12
-        prefill = {"workload": "prefill T=16384, zero bias", "tokens_per_s": pcfg.T / (p_ms / 1000.0),
-                   "ms_per_step": p_ms, "stages_ms": p_stage,
-                   "expert_gemm_tflops": tflops, "peak_bf16_tflops": peaks["bf16"],
-                   "frac_of_bf16_peak": tflops / peaks["bf16"],
-                   "layer_tflops": pcfg.T * FLOP_PER_TOKEN / (p_ms / 1000.0) / 1e12}
-        assert lib.workspace_status(pw.ws) == 0
-        del pw
+        prefill = prefill_figures(lib, mi.CONFIGS["prefill"], weights, dev, flush, peaks,
+                                  args.prefill_steps)
+
+    # ---- NVFP4 experts (the decode weights packed), decode and prefill
+    nvfp4 = None
+    if not args.no_nvfp4:
+        packed = [mi.quantize_experts_nvfp4(w) for w in weights]
+        fp4w = tuple(p[0] for p in packed) + tuple(p[1] for p in packed) + tuple(p[2] for p in packed)
+        nvfp4 = nvfp4_figures(lib, mi, fp4w, dev, flush, peaks, args)
+        del packed, fp4w
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -431,7 +504,7 @@ def main():
                    "T": cfg.T, "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": 10 * args.steps, "stages_ms": stages, "prefill": prefill,
+        "gpu_launches": 10 * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4,
     }
     print(json.dumps(line))
     if dist is not None:

@@ -113,31 +113,49 @@ __device__ __forceinline__ void top2_merge(float &a1, float &a2, float b1, float
   a2 = lo;
 }
 
-// One warp per token.  Lane l holds experts e = l + 32 i, i = 0..7.
+// One CTA per kTopkTokens tokens.  First all 256 threads add the K-split
+// partial logits of the CTA's tokens, every load issued at once (splits added
+// in split order), into shared memory; then one warp per token does the
+// selection.  Lane l holds experts e = l + 32 i, i = 0..7.
+constexpr int kTopkTokens = 8;
+
 __global__ void __launch_bounds__(256) router_topk_kernel(TopkArgs a) {
   constexpr int NS = 8;
+  __shared__ float logits_s[kTopkTokens][256];
   const int lane = threadIdx.x & 31;
   const int gsize = 1 << a.log2_gsize;
-  const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
-    float s[NS], sb[NS];
-    // logits: the K-split partial sums, added in split order (loads issued
-    // four splits ahead so the chain of adds does not serialise the loads)
-    float l[NS];
+  const int t0 = blockIdx.x * kTopkTokens;
+  {
+    const int e = threadIdx.x;  // blockDim.x == 256 >= E
+    float acc[kTopkTokens];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) l[i] = 0.f;
-#pragma unroll 4
-    for (int sp = 0; sp < a.ksplit; ++sp) {
-      const float *row = a.partial + ((size_t)sp * a.T + t) * a.E;
+    for (int j = 0; j < kTopkTokens; ++j) acc[j] = 0.f;
+    if (e < a.E) {
 #pragma unroll
-      for (int i = 0; i < NS; ++i)
-        if (lane + 32 * i < a.E) l[i] += __ldg(row + lane + 32 * i);
+      for (int sp = 0; sp < kMaxRouterSplit; ++sp) {
+        if (sp < a.ksplit) {
+          float v[kTopkTokens];
+#pragma unroll
+          for (int j = 0; j < kTopkTokens; ++j)
+            v[j] = (t0 + j < a.T) ? __ldg(a.partial + ((size_t)sp * a.T + t0 + j) * a.E + e) : 0.f;
+#pragma unroll
+          for (int j = 0; j < kTopkTokens; ++j) acc[j] += v[j];
+        }
+      }
     }
+#pragma unroll
+    for (int j = 0; j < kTopkTokens; ++j) logits_s[j][e] = acc[j];
+  }
+  __syncthreads();
+  const int t = t0 + (threadIdx.x >> 5);
+  if (t < a.T) {
+    float s[NS], sb[NS];
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const int e = lane + 32 * i;
       if (e < a.E) {
-        s[i] = 1.0f / (1.0f + expf(-l[i]));
+        const float l = logits_s[threadIdx.x >> 5][e];
+        s[i] = 1.0f / (1.0f + expf(-l));
         sb[i] = s[i] + a.bias[e];
       } else {
         s[i] = 0.f;
@@ -301,8 +319,7 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
   a.ksplit = rp.ksplit;
   a.log2_gsize = ilog2(d.E / d.n_group);
   a.routed_scale = d.routed_scale;
-  const int blocks = std::max(1, std::min((d.T + 7) / 8, 148 * 16));
-  router_topk_kernel<<<blocks, 256, 0, stream>>>(a);
+  router_topk_kernel<<<(d.T + kTopkTokens - 1) / kTopkTokens, 256, 0, stream>>>(a);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
