@@ -357,7 +357,12 @@ def profile_config(name):
     import moe_inputs as mi
     small = dict(H=5120, E=32, n_group=8, topk_group=4, top_k=8, I=2560, routed_scale=2.5)
     extra = {"prefill-small": mi.MoeConfig("prefill-small", T=4096, bias="zero", **small),
-             "decode-small": mi.MoeConfig("decode-small", T=64, **small)}
+             "decode-small": mi.MoeConfig("decode-small", T=64, **small),
+             "nvfp4-decode": mi.CONFIGS["nvfp4"],
+             "nvfp4-prefill": mi.CONFIGS["nvfp4"].with_T(16384),
+             "nvfp4-decode-small": mi.MoeConfig("nvfp4-decode-small", T=64, weights="nvfp4", **small),
+             "nvfp4-prefill-small": mi.MoeConfig("nvfp4-prefill-small", T=4096, bias="zero",
+                                                 weights="nvfp4", **small)}
     return extra[name] if name in extra else mi.CONFIGS[name]
 
 
@@ -368,6 +373,10 @@ def run_profile(args):
     dev = torch.device("cuda", 0)
     cfg = profile_config(args.profile)
     weights = mi.make_expert_weights(cfg, device=dev)
+    if cfg.weights == "nvfp4":
+        packed = [mi.quantize_experts_nvfp4(w) for w in weights]
+        weights = tuple(p[i] for i in range(3) for p in packed)
+        torch.cuda.empty_cache()
     wl = Workload(lib, cfg, weights, dev, stages=False)
     for _ in range(args.warmup):
         wl.forward(lib)
@@ -389,7 +398,8 @@ def main():
     ap.add_argument("--no-nvfp4", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--profile", choices=["decode", "prefill", "skewed", "prefill-small",
-                                          "decode-small"], default=None,
+                                          "decode-small", "nvfp4-decode", "nvfp4-prefill",
+                                          "nvfp4-decode-small", "nvfp4-prefill-small"], default=None,
                     help="run only warm-up + steps forwards of one workload (for ncu)")
     args = ap.parse_args()
     peaks = load_peaks()

@@ -63,6 +63,7 @@ struct ExpertGemm {
   static constexpr bool CONVERT = false;
   static constexpr bool F16 = false;
   static constexpr int RAW_BYTES = 0;
+  static constexpr int RSTAGES = 0;
   static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 
@@ -189,6 +190,7 @@ struct ExpertGemmTM {
   static constexpr bool CONVERT = false;
   static constexpr bool F16 = false;
   static constexpr int RAW_BYTES = 0;
+  static constexpr int RSTAGES = 0;
   static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 

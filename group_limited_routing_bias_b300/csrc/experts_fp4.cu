@@ -7,11 +7,12 @@
 // six significant bits and lies in [2^-10, 2688], so it is exact in f16; the
 // global scale, a per-matrix constant, is applied to the fp32 accumulator in
 // the epilogue.  The MMAs therefore run kind::f16 with f16 operands: the
-// producer TMA-loads the packed codes and their scales into a raw ring, four
-// converter warps turn each 64-wide K slice into an f16 operand tile with the
-// 128-byte swizzle (hardware e2m1x2 and e4m3x2 conversions, one f16x2
-// multiply per code pair), and the activations (exact bf16 -> f16 copies,
-// made in the dispatch gather) arrive by TMA.  h is kept in f16.
+// producer TMA-loads the packed codes and their scales into a deep raw ring,
+// eight converter warps turn each 64-wide K slice into an f16 operand tile
+// with the 128-byte swizzle (hardware e2m1x2 and e4m3x2 conversions, one
+// f16x2 multiply per code pair) and free the raw slot at once, and the
+// activations (exact bf16 -> f16 copies, made in the dispatch gather) arrive
+// by TMA.  h is kept in f16.
 //
 // Two tile shapes, as for bf16 weights: weights on the MMA's M side for small
 // batches (decode streams each touched expert's packed weights once), and
@@ -29,23 +30,23 @@ constexpr int kPackedRowBytes = kTileK / 2;  // 32 bytes of e2m1 pairs per row p
 constexpr int kScaleBoxBytes = 16;           // one scale box: 16 scales = 256 k = 4 K slices
 constexpr int kRawRowBytes = kPackedRowBytes + kScaleBoxBytes;
 
-// One 64-wide K slice of one weight row: 32 bytes of e2m1 pairs (even k in the
-// low nibble) and the slice's four e4m3 block scales -> 64 f16 values, written
-// as eight 16-byte chunks at the 128-byte-swizzle positions of row r.
-__device__ __forceinline__ void fp4_row_to_f16(const uint8_t *packed, uint32_t scales4,
-                                               uint8_t *dst_row, int r) {
-  const uint4 p0 = *reinterpret_cast<const uint4 *>(packed);
-  const uint4 p1 = *reinterpret_cast<const uint4 *>(packed + 16);
-  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-  uint32_t s2[4];
+// Half of one 64-wide K slice of one weight row: 16 bytes of e2m1 pairs (even
+// k in the low nibble) and the two e4m3 block scales that cover them -> 32 f16
+// values, written as four 16-byte chunks (4*half .. 4*half+3) at the
+// 128-byte-swizzle positions of row r.
+__device__ __forceinline__ void fp4_half_row_to_f16(const uint8_t *packed16, uint32_t scales2,
+                                                    uint8_t *dst_row, int r, int half) {
+  const uint4 p = *reinterpret_cast<const uint4 *>(packed16);
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+  uint32_t s2[2];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t b = (scales4 >> (8 * j)) & 0xFFu;
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t b = (scales2 >> (8 * j)) & 0xFFu;
     const uint16_t pair = (uint16_t)(b | (b << 8));
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2[j]) : "h"(pair));
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     uint32_t o0, o1, o2, o3;
     asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
         "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
@@ -55,12 +56,27 @@ __device__ __forceinline__ void fp4_row_to_f16(const uint8_t *packed, uint32_t s
         "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
         : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
         : "r"(w[i]));
-    const uint32_t sc = s2[i >> 1];  // codes 8i..8i+7 lie in block i/2
+    const uint32_t sc = s2[i >> 1];  // codes 8i..8i+7 of this half lie in block i/2
     asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o0) : "r"(sc));
     asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o1) : "r"(sc));
     asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o2) : "r"(sc));
     asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o3) : "r"(sc));
-    *reinterpret_cast<uint4 *>(dst_row + ((i ^ (r & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
+    const int chunk = 4 * half + i;
+    *reinterpret_cast<uint4 *>(dst_row + ((chunk ^ (r & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
+  }
+}
+
+// Converts the NW weight rows of one raw slot (packed codes [NW][32 B], then
+// scale boxes [NW][16 B]) into the operand tile at dst (row r at r * 128 B):
+// 2 * NW half-row items over the 256 converter threads.
+template <int NW>
+__device__ __forceinline__ void fp4_convert_slot(const uint8_t *raw, uint8_t *dst, int k, int ctid) {
+#pragma unroll
+  for (int it = ctid; it < 2 * NW; it += 32 * kConvertWarps) {
+    const int r = it >> 1, half = it & 1;
+    const uint32_t sc = *reinterpret_cast<const uint16_t *>(
+        raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4 + half * 2);
+    fp4_half_row_to_f16(raw + r * kPackedRowBytes + half * 16, sc, dst + r * 128, r, half);
   }
 }
 
@@ -154,12 +170,14 @@ struct ExpertGemmFP4 {
   static constexpr bool CONVERT = true;
   static constexpr bool F16 = true;
   static constexpr int RAW_BYTES = NW * kRawRowBytes;
-  static constexpr int TX_BYTES = BN * kTileK * 2 + RAW_BYTES;
+  static constexpr int TX_BYTES = BN * kTileK * 2;  // the activation tile; raw bytes on their own ring
   static constexpr int NBUF = (2 * NA * BN <= 512) ? 2 : 1;
-  static constexpr int STAGE_BYTES = StageGeom<BN, NA, RAW_BYTES>::kBytes;
-  static constexpr int STAGES_FIT = (kSmemLimit - kSmemReserve - (int)sizeof(Fp4Sched)) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
-  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static constexpr int OPERAND_BYTES = StageGeom<BN, NA>::kBytes;
+  static constexpr int STAGES = OPERAND_BYTES * 3 <= 110 * 1024 ? 3 : 2;
+  static constexpr int RSTAGES_FIT =
+      (kSmemLimit - kSmemReserve - (int)sizeof(Fp4Sched) - STAGES * OPERAND_BYTES) / RAW_BYTES;
+  static constexpr int RSTAGES = RSTAGES_FIT > 16 ? 16 : RSTAGES_FIT;
+  static_assert(RSTAGES >= 2, "raw ring needs two slots");
 
   using Params = Fp4Params;
   using Sched = Fp4Sched;
@@ -177,25 +195,21 @@ struct ExpertGemmFP4 {
   }
   __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
-    uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
     tma_load_2d(stage + NA * kATileBytes, &p.tmap_act, bar, k * kTileK, t.row0);
-    tma_load_2d(raw, &p.tmap_q0, bar, k * kPackedRowBytes, t.arow0);
-    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, bar, (k >> 2) * kScaleBoxBytes, t.arow0);
+  }
+  __device__ static void load_raw(const Params &p, const Tile &t, int k, uint8_t *raw,
+                                  uint64_t *raw_bar) {
+    tma_load_2d(raw, &p.tmap_q0, raw_bar, k * kPackedRowBytes, t.arow0);
+    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, raw_bar, (k >> 2) * kScaleBoxBytes, t.arow0);
     if (GATEUP) {
-      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, bar, k * kPackedRowBytes, t.arow0);
-      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, bar,
+      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, raw_bar, k * kPackedRowBytes, t.arow0);
+      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, raw_bar,
                   (k >> 2) * kScaleBoxBytes, t.arow0);
     }
   }
-  __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage, int ctid) {
-    const uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
-#pragma unroll
-    for (int i = 0; i < NA; ++i) {
-      const int r = ctid + kTileM * i;
-      const uint32_t sc = *reinterpret_cast<const uint32_t *>(
-          raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4);
-      fp4_row_to_f16(raw + r * kPackedRowBytes, sc, stage + r * 128, r);
-    }
+  __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage,
+                                 const uint8_t *raw, int ctid) {
+    fp4_convert_slot<NW>(raw, stage, k, ctid);  // A tiles: gate rows 0..127, up rows 128..255
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     constexpr int CH = BN < 32 ? BN : 32;
@@ -244,9 +258,13 @@ struct ExpertGemmTMFP4 {
   static constexpr bool CONVERT = true;
   static constexpr bool F16 = true;
   static constexpr int RAW_BYTES = NW * kRawRowBytes;
-  static constexpr int TX_BYTES = kATileBytes + RAW_BYTES;
+  static constexpr int TX_BYTES = kATileBytes;  // the activation tile; raw bytes on their own ring
   static constexpr int NBUF = 2;
   static constexpr int STAGES = 3;
+  static constexpr int RSTAGES_FIT = (kSmemLimit - kSmemReserve - (int)sizeof(Fp4Sched) -
+                                      STAGES * StageGeom<BN, NA>::kBytes) / RAW_BYTES;
+  static constexpr int RSTAGES = RSTAGES_FIT > 16 ? 16 : RSTAGES_FIT;
+  static_assert(RSTAGES >= 2, "raw ring needs two slots");
   static constexpr int FW = GATEUP ? 128 : 256;
 
   using Params = Fp4Params;
@@ -269,26 +287,21 @@ struct ExpertGemmTMFP4 {
   }
   __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
-    uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
     tma_load_2d(stage, &p.tmap_act, bar, k * kTileK, t.row0);
-    tma_load_2d(raw, &p.tmap_q0, bar, k * kPackedRowBytes, t.brow0);
-    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, bar, (k >> 2) * kScaleBoxBytes, t.brow0);
+  }
+  __device__ static void load_raw(const Params &p, const Tile &t, int k, uint8_t *raw,
+                                  uint64_t *raw_bar) {
+    tma_load_2d(raw, &p.tmap_q0, raw_bar, k * kPackedRowBytes, t.brow0);
+    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, raw_bar, (k >> 2) * kScaleBoxBytes, t.brow0);
     if (GATEUP) {
-      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, bar, k * kPackedRowBytes, t.brow0);
-      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, bar,
+      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, raw_bar, k * kPackedRowBytes, t.brow0);
+      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, raw_bar,
                   (k >> 2) * kScaleBoxBytes, t.brow0);
     }
   }
-  __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage, int ctid) {
-    const uint8_t *raw = stage + StageGeom<BN, NA>::kOperandBytes;
-    uint8_t *b = stage + kATileBytes;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int r = ctid + kTileM * i;
-      const uint32_t sc = *reinterpret_cast<const uint32_t *>(
-          raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4);
-      fp4_row_to_f16(raw + r * kPackedRowBytes, sc, b + r * 128, r);
-    }
+  __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage,
+                                 const uint8_t *raw, int ctid) {
+    fp4_convert_slot<NW>(raw, stage + kATileBytes, k, ctid);  // B tile: 256 weight rows
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     const bool valid = row < t.nrows;

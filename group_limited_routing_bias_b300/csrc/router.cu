@@ -59,6 +59,7 @@ struct RouterLogits {
   static constexpr bool CONVERT = false;
   static constexpr bool F16 = false;
   static constexpr int RAW_BYTES = 0;
+  static constexpr int RSTAGES = 0;
   static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
   __device__ static void prologue(const Params &, Sched &) {}

@@ -11,14 +11,20 @@
 // The accumulators are double-buffered in tensor memory when they fit, so
 // the epilogue of one tile overlaps the main loop of the next.
 //
-// Problems whose weights arrive packed (NVFP4) add a converter role:
-//   warps 8..11   : wait for a stage's raw bytes, dequantise them into the
-//                   stage's swizzled operand tile, fence the generic proxy
-//                   against the tensor cores' async proxy, then signal the MMA.
+// Problems whose weights arrive packed (NVFP4) add a converter role and a
+// second ring: warp 0 TMA-loads the packed bytes of each K slice into a deep
+// raw ring (RSTAGES), warp 3 the activation tile into the operand ring;
+//   warps 8..15   : wait for a slice's raw bytes, dequantise them into the
+//                   operand slot's swizzled weight tile, release the raw slot
+//                   at once, fence the generic proxy against the tensor
+//                   cores' async proxy, then signal the MMA.
+// The raw ring is refilled as soon as a slice is converted, so the bytes in
+// flight are not held back by MMA completion.
 //
 // A problem class P supplies the shapes and the tile schedule:
-//   static constexpr int BN, NA, STAGES, NBUF, RAW_BYTES, TX_BYTES;
+//   static constexpr int BN, NA, STAGES, NBUF, TX_BYTES;
 //   static constexpr bool CONVERT, F16;   (packed weights; f16 instead of bf16 operands)
+//   static constexpr int RSTAGES, RAW_BYTES;  (CONVERT: raw ring depth and slot size)
 //   struct Params { ...; uint32_t *status; };  struct Sched;  struct Tile;
 //   static void prologue(const Params&, Sched&)   (all threads; may __syncthreads)
 //   static int  num_tiles(const Params&, const Sched&)
@@ -26,7 +32,11 @@
 //   static int  num_k(const Params&, const Tile&)
 //   static void load(const Params&, const Tile&, int k, uint8_t *stage, uint64_t *bar)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
-//   static void convert(const Params&, const Tile&, int k, uint8_t *stage, int ctid)  (CONVERT)
+//   CONVERT problems load the operand ring's activation tile with load() and the
+//   raw ring with
+//   static void load_raw(const Params&, const Tile&, int k, uint8_t *raw, uint64_t *raw_bar)
+//   static void convert(const Params&, const Tile&, int k, uint8_t *stage, const uint8_t *raw,
+//                       int ctid)   (ctid 0..255)
 #pragma once
 
 #include "ptx.cuh"
@@ -39,26 +49,34 @@ constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
 constexpr int kSmemLimit = 232448;                // 227 KB dynamic shared memory
 constexpr int kSmemReserve = 4096;                // alignment slack + barriers
 
-template <int BN, int NA, int RAW = 0>
+template <int BN, int NA>
 struct StageGeom {
   static constexpr int kOperandBytes = NA * kATileBytes + BN * kTileK * 2;
-  static constexpr int kBytes = kOperandBytes + RAW;
+  static constexpr int kBytes = kOperandBytes;
   static_assert(kBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
 
 template <class P>
 __host__ __device__ constexpr int stage_bytes_of() {
-  return StageGeom<P::BN, P::NA, P::RAW_BYTES>::kBytes;
+  return StageGeom<P::BN, P::NA>::kBytes;
+}
+
+template <class P>
+__host__ __device__ constexpr int raw_ring_bytes_of() {
+  return P::CONVERT ? P::RSTAGES * P::RAW_BYTES : 0;
 }
 
 template <class P>
 __host__ __device__ constexpr int smem_bytes_for() {
-  return kSmemReserve + P::STAGES * stage_bytes_of<P>() + (int)sizeof(typename P::Sched);
+  return kSmemReserve + P::STAGES * stage_bytes_of<P>() + raw_ring_bytes_of<P>() +
+         (int)sizeof(typename P::Sched);
 }
+
+constexpr int kConvertWarps = 8;
 
 template <class P>
 __host__ __device__ constexpr int threads_for() {
-  return P::CONVERT ? 384 : 256;
+  return P::CONVERT ? 256 + 32 * kConvertWarps : 256;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -78,16 +96,20 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *stages = smem_raw + pad;
-  uint64_t *full = reinterpret_cast<uint64_t *>(stages + P::STAGES * STAGE);
+  constexpr int RS = P::CONVERT ? P::RSTAGES : 1;
+  uint8_t *raws = stages + P::STAGES * STAGE;  // raw ring (CONVERT only)
+  uint64_t *full = reinterpret_cast<uint64_t *>(raws + raw_ring_bytes_of<P>());
   uint64_t *empty = full + P::STAGES;
   uint64_t *tfull = empty + P::STAGES;
   uint64_t *tempty = tfull + P::NBUF;
   uint64_t *ready = tempty + P::NBUF;  // converters -> MMA (CONVERT only)
-  uint64_t *drain = ready + P::STAGES;
+  uint64_t *raw_full = ready + P::STAGES;
+  uint64_t *raw_empty = raw_full + RS;
+  uint64_t *drain = raw_empty + RS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  typename P::Sched *sched =
-      reinterpret_cast<typename P::Sched *>(stages + P::STAGES * STAGE + 1024);
+  typename P::Sched *sched = reinterpret_cast<typename P::Sched *>(
+      raws + raw_ring_bytes_of<P>() + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -101,7 +123,11 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
-    for (int s = 0; s < P::STAGES; ++s) mbar_init(&ready[s], 4);
+    for (int s = 0; s < P::STAGES; ++s) mbar_init(&ready[s], kConvertWarps);
+    for (int s = 0; s < RS; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kConvertWarps);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -117,9 +143,13 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   const uint32_t tmem_base = *tmem_slot;
   const int ntiles = P::num_tiles(p, *sched);
 
-  if (warp == 0) {
+  if (warp == 0 || (P::CONVERT && warp == 3)) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producers.  Without conversion warp 0 fills the
+      // operand ring.  With it, warp 0 streams packed weights into the raw ring
+      // (gated only by the converters freeing raw slots) and warp 3 issues the
+      // activation tiles into the operand ring (gated by MMA completion).
+      const bool raw_role = P::CONVERT && warp == 0;
       int stage = 0;
       uint32_t ph = 0, issued = 0, par = 0;
       bool ok = true;
@@ -127,23 +157,42 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
         const typename P::Tile tile = P::tile(p, *sched, t);
         const int nk = P::num_k(p, tile);
         for (int k = 0; k < nk; ++k) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
+          if constexpr (P::CONVERT) {
+            if (raw_role) {
+              if (!mbar_wait(&raw_empty[stage], ph ^ 1u, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&raw_full[stage], P::RAW_BYTES);
+              P::load_raw(p, tile, k, raws + stage * P::RAW_BYTES, &raw_full[stage]);
+            } else {
+              if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&full[stage], P::TX_BYTES);
+              P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
+            }
+          } else {
+            if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], P::TX_BYTES);
+            P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
           }
-          mbar_arrive_expect_tx(&full[stage], P::TX_BYTES);
-          P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
           issued |= 1u << stage;
           par = (par & ~(1u << stage)) | (ph << stage);
-          if (++stage == P::STAGES) {
+          if (++stage == (raw_role ? RS : P::STAGES)) {
             stage = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok) {  // let every copy still in flight land before the CTA exits
-        for (int s = 0; s < P::STAGES; ++s)
-          if (issued & (1u << s)) mbar_drain_wait(&full[s], (par >> s) & 1u);
+        uint64_t *bars = raw_role ? raw_full : full;
+        for (int s = 0; s < (raw_role ? RS : P::STAGES); ++s)
+          if (issued & (1u << s)) mbar_drain_wait(&bars[s], (par >> s) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -162,7 +211,8 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
         tc_fence_after();
         const uint32_t d0 = tmem_base + buf * kAccCols;
         for (int k = 0; k < nk; ++k) {
-          if (!mbar_wait(P::CONVERT ? &ready[stage] : &full[stage], ph, abort_flag, p.status)) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, p.status) ||
+              (P::CONVERT && !mbar_wait(&ready[stage], ph, abort_flag, p.status))) {
             ok = false;
             break;
           }
@@ -200,23 +250,32 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   } else if (P::CONVERT && warp >= 8) {
     // ---------------- converters: raw packed weights -> swizzled operand tile
     const int ctid = threadIdx.x - 256;
-    int stage = 0;
-    uint32_t ph = 0;
+    int stage = 0, rstage = 0;
+    uint32_t ph = 0, rph = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       const typename P::Tile tile = P::tile(p, *sched, t);
       const int nk = P::num_k(p, tile);
       for (int k = 0; k < nk; ++k) {
-        bool got = mbar_wait(&full[stage], ph, abort_flag, p.status);
+        // the raw slice has landed, and the operand slot it goes to is free
+        bool got = mbar_wait(&raw_full[rstage], rph, abort_flag, p.status) &&
+                   mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
           ok = false;
           break;
         }
-        P::convert(p, tile, k, stages + stage * STAGE, ctid);
+        if constexpr (P::CONVERT)
+          P::convert(p, tile, k, stages + stage * STAGE, raws + rstage * P::RAW_BYTES, ctid);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rstage]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ready[stage]);
+        if (++rstage == RS) {
+          rstage = 0;
+          rph ^= 1u;
+        }
         if (++stage == P::STAGES) {
           stage = 0;
           ph ^= 1u;
