@@ -222,10 +222,13 @@ def test_forward_skewed_sampled(lib):
     assert load.max() >= 6 * load.mean()
 
 
-def test_stages_match_forward(lib):
+@pytest.mark.parametrize("T", [150, 2048])
+def test_stages_match_forward(lib, T):
     """moe_route -> moe_permute -> moe_experts_swiglu -> moe_combine equals moe_forward
-    bit for bit, and each y_partial row is its routed expert's output times its weight."""
-    c = mi.CONFIGS["tiny"].with_T(150)
+    bit for bit, and each y_partial row is its routed expert's output times its weight.
+    At T=2048 moe_forward's gate/up GEMM gathers x rows itself while the staged
+    calls read x_perm."""
+    c = mi.CONFIGS["tiny"].with_T(T)
     case = Case(c)
     d = lib.dims_of(c)
     y_fwd, idx_fwd, w_fwd = forward(lib, case)
