@@ -13,7 +13,6 @@
 // projection scales each token row by its routing weight in its epilogue.
 #include "moe_internal.cuh"
 #include "tc_gemm.cuh"
-#include "tc_gemm2.cuh"
 
 namespace beam {
 
@@ -290,113 +289,6 @@ struct ExpertGemmTM {
   }
 };
 
-// Two-CTA token-major expert GEMM (tc_gemm2.cuh): a CTA pair computes 256 token
-// rows of one expert (128 per CTA) against 256 weight rows; each CTA stages
-// its own 128 token rows and half of the weight rows (gate/up: the leader the
-// 128 gate rows, its peer the 128 up rows of the same features; down: 128
-// output features each), so the fp32 accumulator of each CTA still holds g and
-// u of its rows side by side and the epilogue is the one-CTA one.
-template <bool GATEUP>
-struct ExpertGemmTM2 {
-  static constexpr int BN = 256;
-  static constexpr int NBUF = 2;
-  static constexpr int STAGES = 6;
-  static constexpr int FW = GATEUP ? 128 : 256;
-  using Params = typename ExpertGemmTM<GATEUP>::Params;
-  struct Sched {
-    int off[257];
-    int tp[257];  // prefix of pair tiles per expert (256-row token tiles x feature tiles)
-  };
-  struct Tile {
-    int row0, end, brow0, f;  // pair's first row, expert's end row
-  };
-  __device__ static void prologue(const Params &p, Sched &s) {
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.off[i] = p.offsets[i];
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      const int per = (p.E + 31) / 32;
-      const int e0 = lane * per;
-      int local = 0;
-      for (int e = e0; e < e0 + per && e < p.E; ++e)
-        local += (s.off[e + 1] - s.off[e] + 2 * kTileM - 1) / (2 * kTileM) * p.nf;
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int run = incl - local;
-      for (int e = e0; e < e0 + per && e < p.E; ++e) {
-        s.tp[e] = run;
-        run += (s.off[e + 1] - s.off[e] + 2 * kTileM - 1) / (2 * kTileM) * p.nf;
-      }
-      if (lane == 31) s.tp[p.E] = incl;
-    }
-    __syncthreads();
-  }
-  __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E]; }
-  __device__ static Tile tile(const Params &p, const Sched &s, int t) {
-    int lo = 0, hi = p.E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s.tp[mid] <= t) lo = mid;
-      else hi = mid;
-    }
-    const int e = lo;
-    const int npt = (s.off[e + 1] - s.off[e] + 2 * kTileM - 1) / (2 * kTileM);
-    const int local = t - s.tp[e];
-    const int f = local / npt, pt = local - f * npt;
-    return Tile{s.off[e] + pt * 2 * kTileM, s.off[e + 1], e * p.b_rows + f * FW, f};
-  }
-  __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
-  __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint32_t bar,
-                              int rank) {
-    tma_load_2d_cg2(stage, &p.tmap_a, bar, k * kTileK, t.row0 + rank * kTileM);
-    if (GATEUP)
-      tma_load_2d_cg2(stage + kATileBytes, rank == 0 ? &p.tmap_b0 : &p.tmap_b1, bar, k * kTileK,
-                      t.brow0);
-    else
-      tma_load_2d_cg2(stage + kATileBytes, &p.tmap_b0, bar, k * kTileK, t.brow0 + rank * kTileM);
-  }
-  __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row, int rank) {
-    const int row0 = t.row0 + rank * kTileM;
-    typename ExpertGemmTM<GATEUP>::Tile one;
-    one.row0 = row0;
-    one.nrows = max(0, min(kTileM, t.end - row0));
-    one.brow0 = t.brow0;
-    one.f = t.f;
-    ExpertGemmTM<GATEUP>::epilogue(p, one, taddr, row);
-  }
-};
-
-template <class P>
-moe_status launch_gemm2(const typename P::Params &prm, int grid, cudaStream_t stream) {
-  constexpr int smem = smem_bytes_cg2<P>();
-  static_assert(smem <= kSmemLimit, "shared memory budget");
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm2_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tc_gemm2_kernel<P>, prm) != cudaSuccess) return MOE_ERR_CUDA;
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
 template <class P>
 moe_status launch_gemm(const typename P::Params &prm, int grid, cudaStream_t stream) {
   constexpr int smem = smem_bytes_for<P>();
@@ -467,14 +359,14 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
                                       const float *topk_w, void *y_partial, __nv_bfloat16 *h,
                                       uint32_t *status, cudaStream_t stream) {
   const long Tk = (long)d.T * d.top_k;
-  const long max_pt = Tk / (2 * kTileM) + std::min<long>(d.E, Tk);  // pair tiles per feature tile
-  const int pairs = std::max(1, device_sm_count() / 2);
+  const long max_tt = Tk / kTileM + std::min<long>(d.E, Tk);
+  const int sms = device_sm_count();
   {
-    using P = ExpertGemmTM2<true>;
+    using P = ExpertGemmTM<true>;
     typename P::Params prm;
     if (!make_tmap_bf16_2d(&prm.tmap_a, x_perm, d.H, Tk, kTileM) ||
-        !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_gate, d.H, (uint64_t)d.E * d.I, kTileM) ||
-        !make_tmap_bf16_2d(&prm.tmap_b1, ex.w_up, d.H, (uint64_t)d.E * d.I, kTileM))
+        !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_gate, d.H, (uint64_t)d.E * d.I, 128) ||
+        !make_tmap_bf16_2d(&prm.tmap_b1, ex.w_up, d.H, (uint64_t)d.E * d.I, 128))
       return MOE_ERR_CUDA;
     prm.offsets = offsets;
     prm.row_src = row_src;
@@ -486,15 +378,15 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
     prm.ksteps = d.H / kTileK;
     prm.nf = d.I / P::FW;
     prm.status = status;
-    const int grid = 2 * (int)std::max<long>(1, std::min<long>(pairs, max_pt * prm.nf));
-    const moe_status st = launch_gemm2<P>(prm, grid, stream);
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.nf));
+    const moe_status st = launch_gemm<P>(prm, grid, stream);
     if (st != MOE_OK) return st;
   }
   {
-    using P = ExpertGemmTM2<false>;
+    using P = ExpertGemmTM<false>;
     typename P::Params prm;
     if (!make_tmap_bf16_2d(&prm.tmap_a, h, d.I, Tk, kTileM) ||
-        !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_down, d.I, (uint64_t)d.E * d.H, kTileM))
+        !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_down, d.I, (uint64_t)d.E * d.H, 256))
       return MOE_ERR_CUDA;
     prm.tmap_b1 = prm.tmap_b0;
     prm.offsets = offsets;
@@ -507,8 +399,8 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
     prm.ksteps = d.I / kTileK;
     prm.nf = d.H / P::FW;
     prm.status = status;
-    const int grid = 2 * (int)std::max<long>(1, std::min<long>(pairs, max_pt * prm.nf));
-    return launch_gemm2<P>(prm, grid, stream);
+    const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.nf));
+    return launch_gemm<P>(prm, grid, stream);
   }
 }
 
