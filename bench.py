@@ -260,6 +260,22 @@ def nvfp4_figures(lib, mi, fp4w, dev, flush, peaks, args):
     return out
 
 
+# ---------------------------------------------------------------- replicas
+
+
+def aggregate_replicas(ms_local: float, tokens_per_replica: int, world: int, dist=None,
+                       device=None):
+    """Whole-job figures of N independent replicas: the step time is the slowest
+    rank's (max over ranks, one all-reduce of a scalar; no data is exchanged),
+    and the value counts every rank's tokens over that time."""
+    ms = ms_local
+    if dist is not None and world > 1:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_per_replica / (ms / 1000.0)
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 
@@ -449,12 +465,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
-    ms = statistics.mean(per_step)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * cfg.T / (ms / 1000.0)
+    ms, value = aggregate_replicas(statistics.mean(per_step), cfg.T, world, dist, dev)
     assert lib.workspace_status(wl.ws) == 0, "device status set during the timed steps"
 
     if rank != 0:
