@@ -27,7 +27,8 @@ MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
 
 EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
             "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
-            "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_permute_noalloc")
+            "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_bias_update",
+            "moe_permute_noalloc")
 
 
 class MoeDims(ctypes.Structure):
@@ -57,6 +58,7 @@ _sig = {
     "moe_experts_swiglu": ([_DP, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "moe_combine": ([_DP, _P, _P, _P, _P], _I),
     "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
+    "moe_bias_update": ([_DP, _P, _P, ctypes.c_double, _I, _I, ctypes.POINTER(ctypes.c_float), _P], _I),
     "moe_permute_noalloc": ([_DP, _P, _P, _P, _P, _P, _P, _P], _I),
 }
 _native = None
@@ -253,6 +255,17 @@ def moe_forward(d: MoeDims, x, w_router, bias, experts: Experts, y, ws, topk_idx
         ctypes.byref(ex), _ptr(y, torch.bfloat16, (T, H), "y"),
         _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
         _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
+
+
+def moe_bias_update(d: MoeDims, topk_idx, bias, gamma_max: float, step: int, total_steps: int,
+                    stream=None) -> float:
+    """Auxiliary-loss-free bias update, in place on bias fp32 [E]; returns gamma_t."""
+    g = ctypes.c_float(0.0)
+    _check("moe_bias_update", native().moe_bias_update(
+        ctypes.byref(d), _ptr(topk_idx, torch.int32, (d.T, d.top_k), "topk_idx"),
+        _ptr(bias, torch.float32, (d.E,), "bias"), float(gamma_max), int(step), int(total_steps),
+        ctypes.byref(g), _stream(stream)))
+    return g.value
 
 
 def moe_permute_noalloc(d: MoeDims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src,

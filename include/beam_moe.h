@@ -196,6 +196,25 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
                        float *topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Auxiliary-loss-free load balancing ("Beam 1.0": the router's per-expert bias
+ * follows DeepSeek-V3's auxiliary-loss-free balancing with a cosine decay of
+ * the expert-bias updates).  After a batch is routed (topk_idx [T,k] from
+ * moe_route or moe_forward), moves every expert's selection bias one step
+ * against its load:
+ *   load_e  = number of entries of topk_idx equal to e
+ *   gamma_t = gamma_max * (1 + cos(pi * step / total_steps)) / 2,
+ *             step clamped to [0, total_steps]
+ *   bias[e] += gamma_t * sign(T*k/E - load_e)      (sign(0) = 0)
+ * The page names the method, not the formula: this is the plain reading.
+ * bias fp32 [E] is updated in place on `stream`; *gamma_used (nullable)
+ * receives gamma_t as applied (fp32).  Entries outside [0, E) are ignored.
+ * Needs no workspace; results do not depend on thread timing.
+ */
+moe_status moe_bias_update(const moe_dims *dims, const int32_t *topk_idx, float *bias,
+                           double gamma_max, int step, int total_steps, float *gamma_used,
+                           moe_stream_t stream);
+
+/*
  * moe_permute_noalloc — the dispatch of moe_permute for callers that cannot
  * allocate device memory at all: a plug-in inside a host framework that owns
  * every device buffer and passes it only its inputs and outputs, or a serving

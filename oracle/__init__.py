@@ -62,6 +62,8 @@ def _load():
     lib.oracle_decode_matrix.restype = i
     lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e2m1_value.restype = d
+    lib.oracle_bias_update.argtypes = [i, i, i, P, P, d, i, i]
+    lib.oracle_bias_update.restype = f
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = d
     _lib = lib
@@ -231,3 +233,15 @@ def moe_forward(x_bf16, w_router, bias, get_expert: ExpertFn, n_group: int, topk
     r = route(x_bf16, w_router, bias, n_group, topk_group, top_k, routed_scale, details)
     y = experts_forward(x_bf16, r.idx, r.w, get_expert, tokens)
     return y, r
+
+
+def bias_update(topk_idx: np.ndarray, bias: np.ndarray, E: int, gamma_max: float, step: int,
+                total_steps: int):
+    """Auxiliary-loss-free bias update (readings in moe_oracle.c).  Returns
+    (new bias fp32 [E], gamma_t used)."""
+    lib = _load()
+    idx = _c(topk_idx, np.int32)
+    b = np.array(bias, dtype=np.float32, copy=True)
+    T, k = idx.shape
+    g = lib.oracle_bias_update(T, k, E, _ptr(idx), _ptr(b), gamma_max, step, total_steps)
+    return b, g

@@ -33,6 +33,7 @@
  *
  * Parity pins for every function are in tests/test_oracle_*.py.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -293,4 +294,40 @@ int oracle_combine(int T, int top_k, int H, const float *topk_w, const double *o
     }
   }
   return ORACLE_OK;
+}
+
+/* ---- auxiliary-loss-free balancing ------------------------------------ */
+
+/*
+ * One update of the per-expert selection bias ("Beam 1.0": DeepSeek-V3's
+ * auxiliary-loss-free balancing with a cosine decay of the bias updates).
+ * Readings: an expert's load is the number of (token, slot) entries routed
+ * to it in the batch; the mean load is T*k/E; the step size is
+ *   gamma_t = gamma_max * (1 + cos(pi * step / total_steps)) / 2,
+ * step clamped to [0, total_steps]; and
+ *   bias[e] += gamma_t * sign(mean_load - load_e)     (sign(0) = 0),
+ * i.e. underloaded experts are raised, overloaded ones lowered.  gamma_t is
+ * computed in fp64 and rounded once to fp32; each update is one fp32 addition.
+ * Returns gamma_t (as used, fp32).
+ */
+float oracle_bias_update(int T, int top_k, int E, const int32_t *topk_idx, float *bias,
+                         double gamma_max, int step, int total_steps) {
+  double frac = total_steps > 0 ? (double)step / (double)total_steps : 1.0;
+  if (frac < 0.0) frac = 0.0;
+  if (frac > 1.0) frac = 1.0;
+  const float gamma = (float)(gamma_max * 0.5 * (1.0 + cos(M_PI * frac)));
+  long *load = (long *)calloc((size_t)E, sizeof(long));
+  if (!load) return NAN;
+  for (long n = 0; n < (long)T * top_k; ++n) {
+    int e = topk_idx[n];
+    if (e >= 0 && e < E) load[e] += 1;
+  }
+  const double mean = (double)T * top_k / (double)E;
+  for (int e = 0; e < E; ++e) {
+    const double diff = mean - (double)load[e];
+    const float sgn = diff > 0 ? 1.0f : (diff < 0 ? -1.0f : 0.0f);
+    bias[e] = bias[e] + gamma * sgn;
+  }
+  free(load);
+  return gamma;
 }
