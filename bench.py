@@ -199,6 +199,7 @@ def e2e_steps(lib, wl, steps, flush):
 
 
 FP4_EXPERT_BYTES = 3 * (5120 * 2560 // 2 + 5120 * 2560 // 16) + 3 * 4  # codes + e4m3 scales + globals
+FP8_EXPERT_BYTES = 3 * 5120 * 2560 + (2 * 2560 + 5120) * 4              # e4m3 codes + row scales
 
 
 def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
@@ -231,13 +232,14 @@ def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
     return out
 
 
-def nvfp4_figures(lib, mi, fp4w, dev, flush, peaks, args):
-    """NVFP4 experts: decode T=64 (HBM-bound: packed bytes of touched experts) and
-    prefill T=16384 (W4A16: the bf16 tensor peak is its denominator)."""
+def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks):
+    """Packed experts (NVFP4 or FP8): decode T=64 (HBM-bound: packed bytes of
+    touched experts) and prefill T=16384 (W4A16 / W8A16: the bf16 tensor peak
+    is its denominator)."""
     out = {}
     for name, T, steps in (("decode", 64, 50), ("prefill", 16384, 5)):
-        cfg = mi.CONFIGS["nvfp4"].with_T(T)
-        wl = Workload(lib, cfg, fp4w, dev)
+        cfg = mi.CONFIGS[fmt].with_T(T)
+        wl = Workload(lib, cfg, wts, dev)
         for _ in range(3):
             wl.forward(lib)
         torch.cuda.synchronize()
@@ -248,7 +250,7 @@ def nvfp4_figures(lib, mi, fp4w, dev, flush, peaks, args):
         fig = {"T": T, "tokens_per_s": T / (ms / 1000.0), "ms_per_step": ms, "stages_ms": st,
                "touched_experts": touched}
         if name == "decode":
-            gbs = touched * FP4_EXPERT_BYTES / (st["experts"] / 1000.0) / 1e9
+            gbs = touched * expert_bytes / (st["experts"] / 1000.0) / 1e9
             fig.update({"expert_gemm_gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm"],
                         "frac_of_8tbs_nominal": gbs / 8000.0})
         else:
@@ -375,6 +377,7 @@ def profile_config(name):
     extra = {"prefill-small": mi.MoeConfig("prefill-small", T=4096, bias="zero", **small),
              "decode-small": mi.MoeConfig("decode-small", T=64, **small),
              "nvfp4-decode": mi.CONFIGS["nvfp4"],
+             "fp8-decode": mi.CONFIGS["fp8"],
              "nvfp4-prefill": mi.CONFIGS["nvfp4"].with_T(16384),
              "nvfp4-decode-small": mi.MoeConfig("nvfp4-decode-small", T=64, weights="nvfp4", **small),
              "nvfp4-prefill-small": mi.MoeConfig("nvfp4-prefill-small", T=4096, bias="zero",
@@ -392,6 +395,10 @@ def run_profile(args):
     if cfg.weights == "nvfp4":
         packed = [mi.quantize_experts_nvfp4(w) for w in weights]
         weights = tuple(p[i] for i in range(3) for p in packed)
+        torch.cuda.empty_cache()
+    elif cfg.weights == "fp8":
+        packed = [mi.quantize_experts_fp8(w) for w in weights]
+        weights = tuple(p[0] for p in packed) + (None, None, None) + tuple(p[1] for p in packed)
         torch.cuda.empty_cache()
     wl = Workload(lib, cfg, weights, dev, stages=False)
     for _ in range(args.warmup):
@@ -415,7 +422,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--profile", choices=["decode", "prefill", "skewed", "prefill-small",
                                           "decode-small", "nvfp4-decode", "nvfp4-prefill",
-                                          "nvfp4-decode-small", "nvfp4-prefill-small"], default=None,
+                                          "nvfp4-decode-small", "nvfp4-prefill-small",
+                                          "fp8-decode"], default=None,
                     help="run only warm-up + steps forwards of one workload (for ncu)")
     args = ap.parse_args()
     peaks = load_peaks()
@@ -504,13 +512,19 @@ def main():
         prefill = prefill_figures(lib, mi.CONFIGS["prefill"], weights, dev, flush, peaks,
                                   args.prefill_steps)
 
-    # ---- NVFP4 experts (the decode weights packed), decode and prefill
-    nvfp4 = None
+    # ---- packed experts (the decode weights packed to NVFP4 and to FP8), decode and prefill
+    nvfp4 = fp8 = None
     if not args.no_nvfp4:
         packed = [mi.quantize_experts_nvfp4(w) for w in weights]
         fp4w = tuple(p[0] for p in packed) + tuple(p[1] for p in packed) + tuple(p[2] for p in packed)
-        nvfp4 = nvfp4_figures(lib, mi, fp4w, dev, flush, peaks, args)
+        nvfp4 = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks)
         del packed, fp4w
+        torch.cuda.empty_cache()
+        packed = [mi.quantize_experts_fp8(w) for w in weights]
+        fp8w = tuple(p[0] for p in packed) + (None, None, None) + tuple(p[1] for p in packed)
+        fp8 = packed_figures(lib, mi, "fp8", fp8w, FP8_EXPERT_BYTES, dev, flush, peaks)
+        del packed, fp8w
+        torch.cuda.empty_cache()
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -525,7 +539,7 @@ def main():
                    "T": cfg.T, "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": 10 * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4,
+        "gpu_launches": 10 * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4, "fp8": fp8,
     }
     print(json.dumps(line))
     if dist is not None:

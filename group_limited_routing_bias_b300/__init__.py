@@ -21,7 +21,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
 
 MOE_OK = 0
-MOE_W_BF16, MOE_W_NVFP4 = 0, 1
+MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8 = 0, 1, 2
 MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_EXPERTS, MOE_OP_FORWARD = 0, 1, 2, 3
 MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
 
@@ -165,6 +165,7 @@ class Experts:
 
     bf16: w_gate, w_up [E, I, H], w_down [E, H, I].
     NVFP4: w_* packed e2m1 uint8 [E, N, K/2], s_* e4m3 uint8 [E, N, K/16], g_* fp32 [E].
+    FP8: w_* e4m3 uint8 [E, N, K], s_* None, g_* fp32 [E, N] row scales.
     """
     w_gate: torch.Tensor
     w_up: torch.Tensor
@@ -178,7 +179,9 @@ class Experts:
 
     @property
     def dtype(self) -> int:
-        return MOE_W_NVFP4 if self.w_gate.dtype == torch.uint8 else MOE_W_BF16
+        if self.w_gate.dtype != torch.uint8:
+            return MOE_W_BF16
+        return MOE_W_NVFP4 if self.s_gate is not None else MOE_W_FP8
 
     def struct(self, d: MoeDims) -> MoeExperts:
         E, H, I = d.E, d.H, d.I
@@ -189,6 +192,13 @@ class Experts:
                               _ptr(self.w_down, bf, (E, H, I), "w_down"), None, None, None, None,
                               None, None)
         u8, f32 = torch.uint8, torch.float32
+        if self.dtype == MOE_W_FP8:
+            return MoeExperts(MOE_W_FP8, _ptr(self.w_gate, u8, (E, I, H), "w_gate"),
+                              _ptr(self.w_up, u8, (E, I, H), "w_up"),
+                              _ptr(self.w_down, u8, (E, H, I), "w_down"), None, None, None,
+                              _ptr(self.g_gate, f32, (E, I), "g_gate"),
+                              _ptr(self.g_up, f32, (E, I), "g_up"),
+                              _ptr(self.g_down, f32, (E, H), "g_down"))
         return MoeExperts(MOE_W_NVFP4,
                           _ptr(self.w_gate, u8, (E, I, H // 2), "w_gate"),
                           _ptr(self.w_up, u8, (E, I, H // 2), "w_up"),

@@ -127,6 +127,12 @@ moe_status check_experts(const moe_dims *d, const moe_experts *ex) {
     if (d->H % 256 != 0 || d->I % 256 != 0) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
   }
+  if (ex->dtype == MOE_W_FP8) {
+    if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down})) return MOE_ERR_INVALID_ARG;
+    for (const float *g : {ex->g_gate, ex->g_up, ex->g_down})
+      if (!g || (reinterpret_cast<uintptr_t>(g) & 3u)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+  }
   return MOE_ERR_INVALID_ARG;
 }
 
@@ -153,7 +159,7 @@ moe_status moe_check_dims(const moe_dims *dims) { return check_dims(dims); }
 
 size_t moe_workspace_size(const moe_dims *dims, moe_wdtype wdtype, moe_op op) {
   if (check_dims(dims) != MOE_OK) return 0;
-  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_NVFP4) return 0;
+  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_NVFP4 && wdtype != MOE_W_FP8) return 0;
   if (op < MOE_OP_ROUTE || op > MOE_OP_FORWARD) return 0;
   return ws_layout(*dims, op, wdtype).total;
 }
@@ -215,7 +221,7 @@ moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts, 
   if ((st = check_ws(dims, MOE_OP_EXPERTS, ws, ws_bytes, experts->dtype)) != MOE_OK) return st;
   const WsLayout L = ws_layout(*dims, MOE_OP_EXPERTS, experts->dtype);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (experts->dtype == MOE_W_NVFP4) {
+  if (experts->dtype != MOE_W_BF16) {
     void *x16 = at<void>(ws, L.x16);
     const size_t n = (size_t)dims->T * dims->top_k * dims->H;
     if ((st = launch_bf16_to_f16(x_perm, x16, n, s)) != MOE_OK) return st;
@@ -248,7 +254,7 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   if ((st = check_ws(dims, MOE_OP_FORWARD, ws, ws_bytes, experts->dtype)) != MOE_OK) return st;
   const moe_dims &d = *dims;
   const WsLayout L = ws_layout(d, MOE_OP_FORWARD, experts->dtype);
-  const bool fp4 = experts->dtype == MOE_W_NVFP4;
+  const bool fp4 = experts->dtype != MOE_W_BF16;  // packed weights: NVFP4 or FP8
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t *idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
   float *w = topk_w ? topk_w : at<float>(ws, L.topk_w);

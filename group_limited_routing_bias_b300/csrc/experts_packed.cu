@@ -1,12 +1,19 @@
-// Expert MLPs with NVFP4 weights ("Reflection Releases Beam ...", section
-// "Where Beam Saves and Where the Memory Bill Comes In": an NVFP4 checkpoint
-// for Blackwell).  A weight is e2m1(code) * e4m3(block scale) * fp32 global,
-// one scale per 16 consecutive k, one global per expert and matrix.
+// Expert MLPs with packed low-precision weights ("Reflection Releases Beam
+// ...", section "Where Beam Saves and Where the Memory Bill Comes In": BF16,
+// FP8 and NVFP4 checkpoints; NVFP4 for Blackwell).
+//   NVFP4: a weight is e2m1(code) * e4m3(block scale) * fp32 global, one scale
+//          per 16 consecutive k, one global per expert and matrix.
+//   FP8:   a weight is e4m3(code) * fp32 row scale, one scale per output row
+//          (the pages give no FP8 layout; a per-row scale keeps the
+//          dequantisation exact, since it factors out of the K sum).
+// Both formats follow the same pipeline below; a format policy supplies the
+// raw-slot layout, the raw loads, the converter and the epilogue scale.
 //
 // The activations stay 16-bit (W4A16).  The product e2m1 * e4m3 has at most
 // six significant bits and lies in [2^-10, 2688], so it is exact in f16; the
 // global scale, a per-matrix constant, is applied to the fp32 accumulator in
-// the epilogue.  The MMAs therefore run kind::f16 with f16 operands: the
+// the epilogue (for FP8 the row scale does the same job, and e4m3 is exact
+// in f16).  The MMAs therefore run kind::f16 with f16 operands: the
 // producer TMA-loads the packed codes and their scales into a deep raw ring,
 // eight converter warps turn each 64-wide K slice into an f16 operand tile
 // with the 128-byte swizzle (hardware e2m1x2 and e4m3x2 conversions, one
@@ -26,9 +33,9 @@ namespace beam {
 
 namespace {
 
-constexpr int kPackedRowBytes = kTileK / 2;  // 32 bytes of e2m1 pairs per row per K slice
-constexpr int kScaleBoxBytes = 16;           // one scale box: 16 scales = 256 k = 4 K slices
-constexpr int kRawRowBytes = kPackedRowBytes + kScaleBoxBytes;
+constexpr int kPackedRowBytes = kTileK / 2;  // NVFP4: 32 bytes of e2m1 pairs per row per K slice
+constexpr int kScaleBoxBytes = 16;           // NVFP4: one scale box = 16 scales = 256 k = 4 K slices
+constexpr int kFp8RowBytes = kTileK;         // FP8: 64 e4m3 codes per row per K slice
 
 // Half of one 64-wide K slice of one weight row: 16 bytes of e2m1 pairs (even
 // k in the low nibble) and the two e4m3 block scales that cover them -> 32 f16
@@ -66,19 +73,71 @@ __device__ __forceinline__ void fp4_half_row_to_f16(const uint8_t *packed16, uin
   }
 }
 
-// Converts the NW weight rows of one raw slot (packed codes [NW][32 B], then
-// scale boxes [NW][16 B]) into the operand tile at dst (row r at r * 128 B):
-// 2 * NW half-row items over the 256 converter threads.
-template <int NW>
-__device__ __forceinline__ void fp4_convert_slot(const uint8_t *raw, uint8_t *dst, int k, int ctid) {
+// Half of one 64-wide K slice of one FP8 weight row: 32 e4m3 codes -> 32 f16
+// (exact), four 16-byte chunks at the swizzle positions of row r.
+__device__ __forceinline__ void fp8_half_row_to_f16(const uint8_t *codes32, uint8_t *dst_row, int r,
+                                                    int half) {
+  const uint4 a = *reinterpret_cast<const uint4 *>(codes32);
+  const uint4 b = *reinterpret_cast<const uint4 *>(codes32 + 16);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-  for (int it = ctid; it < 2 * NW; it += 32 * kConvertWarps) {
-    const int r = it >> 1, half = it & 1;
-    const uint32_t sc = *reinterpret_cast<const uint16_t *>(
-        raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4 + half * 2);
-    fp4_half_row_to_f16(raw + r * kPackedRowBytes + half * 16, sc, dst + r * 128, r, half);
+  for (int i = 0; i < 4; ++i) {  // chunk i: codes 8i..8i+7 = words 2i, 2i+1
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t word = w[2 * i + j];
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * j]) : "h"((uint16_t)(word & 0xFFFFu)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * j + 1]) : "h"((uint16_t)(word >> 16)));
+    }
+    const int chunk = 4 * half + i;
+    *reinterpret_cast<uint4 *>(dst_row + ((chunk ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
+
+struct Fp4Params;
+
+// NVFP4: raw slot = codes [NW][32 B], then scale boxes [NW][16 B]; the epilogue
+// scale is the expert's global.
+struct Nvfp4Format {
+  static constexpr bool kPerRowScale = false;
+  static constexpr int kRawRowBytes = kPackedRowBytes + kScaleBoxBytes;
+  template <int NW>
+  __device__ static void load_rows(uint8_t *raw, int first_row, const CUtensorMap *q,
+                                   const CUtensorMap *s, uint64_t *bar, int k, int wrow) {
+    tma_load_2d(raw + first_row * kPackedRowBytes, q, bar, k * kPackedRowBytes, wrow);
+    tma_load_2d(raw + NW * kPackedRowBytes + first_row * kScaleBoxBytes, s, bar,
+                (k >> 2) * kScaleBoxBytes, wrow);
+  }
+  template <int NW>
+  __device__ static void convert(const uint8_t *raw, uint8_t *dst, int k, int ctid) {
+#pragma unroll
+    for (int it = ctid; it < 2 * NW; it += 32 * kConvertWarps) {
+      const int r = it >> 1, half = it & 1;
+      const uint32_t sc = *reinterpret_cast<const uint16_t *>(
+          raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4 + half * 2);
+      fp4_half_row_to_f16(raw + r * kPackedRowBytes + half * 16, sc, dst + r * 128, r, half);
+    }
+  }
+};
+
+// FP8: raw slot = codes [NW][64 B]; the epilogue scale is per output row.
+struct Fp8Format {
+  static constexpr bool kPerRowScale = true;
+  static constexpr int kRawRowBytes = kFp8RowBytes;
+  template <int NW>
+  __device__ static void load_rows(uint8_t *raw, int first_row, const CUtensorMap *q,
+                                   const CUtensorMap *, uint64_t *bar, int k, int wrow) {
+    tma_load_2d(raw + first_row * kFp8RowBytes, q, bar, k * kFp8RowBytes, wrow);
+  }
+  template <int NW>
+  __device__ static void convert(const uint8_t *raw, uint8_t *dst, int, int ctid) {
+#pragma unroll
+    for (int it = ctid; it < 2 * NW; it += 32 * kConvertWarps) {
+      const int r = it >> 1, half = it & 1;
+      fp8_half_row_to_f16(raw + r * kFp8RowBytes + half * 32, dst + r * 128, r, half);
+    }
+  }
+};
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
@@ -150,8 +209,9 @@ struct Fp4Params {
   CUtensorMap tmap_q1;   // packed codes of W_up (gate/up only)
   CUtensorMap tmap_s0;   // e4m3 scales [E*N, K/16] of W_gate or W_down
   CUtensorMap tmap_s1;   // scales of W_up
-  const float *g0;       // global scales [E]: gate or down
-  const float *g1;       // global scales [E]: up
+  const float *g0;       // NVFP4: global scales [E] (gate or down); FP8: row scales [E, N]
+  const float *g1;       // the same for up
+  int scale_rows;        // N for FP8 row scales (index e * N + n), 0 for NVFP4 (index e)
   const int32_t *offsets;
   const int32_t *row_src;
   const float *topk_w;
@@ -162,14 +222,18 @@ struct Fp4Params {
 
 // ---------------------------------------------------------------- weights on M (small batches)
 
-template <int BN_, bool GATEUP>
+__device__ __forceinline__ float weight_scale(const float *g, int scale_rows, int e, int n) {
+  return __ldg(g + (size_t)e * (scale_rows > 0 ? scale_rows : 1) + (scale_rows > 0 ? n : 0));
+}
+
+template <class Fmt, int BN_, bool GATEUP>
 struct ExpertGemmFP4 {
   static constexpr int BN = BN_;
   static constexpr int NA = GATEUP ? 2 : 1;
   static constexpr int NW = NA * kTileM;  // weight rows dequantised per stage
   static constexpr bool CONVERT = true;
   static constexpr bool F16 = true;
-  static constexpr int RAW_BYTES = NW * kRawRowBytes;
+  static constexpr int RAW_BYTES = NW * Fmt::kRawRowBytes;
   static constexpr int TX_BYTES = BN * kTileK * 2;  // the activation tile; raw bytes on their own ring
   static constexpr int NBUF = (2 * NA * BN <= 512) ? 2 : 1;
   static constexpr int OPERAND_BYTES = StageGeom<BN, NA>::kBytes;
@@ -199,23 +263,18 @@ struct ExpertGemmFP4 {
   }
   __device__ static void load_raw(const Params &p, const Tile &t, int k, uint8_t *raw,
                                   uint64_t *raw_bar) {
-    tma_load_2d(raw, &p.tmap_q0, raw_bar, k * kPackedRowBytes, t.arow0);
-    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, raw_bar, (k >> 2) * kScaleBoxBytes, t.arow0);
-    if (GATEUP) {
-      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, raw_bar, k * kPackedRowBytes, t.arow0);
-      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, raw_bar,
-                  (k >> 2) * kScaleBoxBytes, t.arow0);
-    }
+    Fmt::template load_rows<NW>(raw, 0, &p.tmap_q0, &p.tmap_s0, raw_bar, k, t.arow0);
+    if (GATEUP) Fmt::template load_rows<NW>(raw, kTileM, &p.tmap_q1, &p.tmap_s1, raw_bar, k, t.arow0);
   }
   __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage,
                                  const uint8_t *raw, int ctid) {
-    fp4_convert_slot<NW>(raw, stage, k, ctid);  // A tiles: gate rows 0..127, up rows 128..255
+    Fmt::template convert<NW>(raw, stage, k, ctid);  // A tiles: gate rows 0..127, up rows 128..255
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     constexpr int CH = BN < 32 ? BN : 32;
     const int f = t.m * kTileM + row;
-    const float ga = __ldg(p.g0 + t.e);
-    const float gb = GATEUP ? __ldg(p.g1 + t.e) : 0.f;
+    const float ga = weight_scale(p.g0, p.scale_rows, t.e, f);
+    const float gb = GATEUP ? weight_scale(p.g1, p.scale_rows, t.e, f) : 0.f;
     for (int c = 0; c < t.nrows; c += CH) {
       uint32_t a[CH];
       tmem_ld_n<CH>(taddr + c, a);
@@ -250,14 +309,14 @@ struct ExpertGemmFP4 {
 
 // ---------------------------------------------------------------- token rows on M (large batches)
 
-template <bool GATEUP>
+template <class Fmt, bool GATEUP>
 struct ExpertGemmTMFP4 {
   static constexpr int BN = 256;
   static constexpr int NA = 1;
   static constexpr int NW = 256;
   static constexpr bool CONVERT = true;
   static constexpr bool F16 = true;
-  static constexpr int RAW_BYTES = NW * kRawRowBytes;
+  static constexpr int RAW_BYTES = NW * Fmt::kRawRowBytes;
   static constexpr int TX_BYTES = kATileBytes;  // the activation tile; raw bytes on their own ring
   static constexpr int NBUF = 2;
   static constexpr int STAGES = 3;
@@ -291,24 +350,22 @@ struct ExpertGemmTMFP4 {
   }
   __device__ static void load_raw(const Params &p, const Tile &t, int k, uint8_t *raw,
                                   uint64_t *raw_bar) {
-    tma_load_2d(raw, &p.tmap_q0, raw_bar, k * kPackedRowBytes, t.brow0);
-    tma_load_2d(raw + NW * kPackedRowBytes, &p.tmap_s0, raw_bar, (k >> 2) * kScaleBoxBytes, t.brow0);
     if (GATEUP) {
-      tma_load_2d(raw + kTileM * kPackedRowBytes, &p.tmap_q1, raw_bar, k * kPackedRowBytes, t.brow0);
-      tma_load_2d(raw + NW * kPackedRowBytes + kTileM * kScaleBoxBytes, &p.tmap_s1, raw_bar,
-                  (k >> 2) * kScaleBoxBytes, t.brow0);
+      Fmt::template load_rows<NW>(raw, 0, &p.tmap_q0, &p.tmap_s0, raw_bar, k, t.brow0);
+      Fmt::template load_rows<NW>(raw, kTileM, &p.tmap_q1, &p.tmap_s1, raw_bar, k, t.brow0);
+    } else {
+      Fmt::template load_rows<NW>(raw, 0, &p.tmap_q0, &p.tmap_s0, raw_bar, k, t.brow0);
     }
   }
   __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage,
                                  const uint8_t *raw, int ctid) {
-    fp4_convert_slot<NW>(raw, stage + kATileBytes, k, ctid);  // B tile: 256 weight rows
+    Fmt::template convert<NW>(raw, stage + kATileBytes, k, ctid);  // B tile: 256 weight rows
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     const bool valid = row < t.nrows;
-    const float ga = __ldg(p.g0 + t.e);
+    const int n0 = t.f * FW;  // first output feature of the tile
     if (GATEUP) {
-      const float gb = __ldg(p.g1 + t.e);
-      __half *dst = static_cast<__half *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + t.f * FW;
+      __half *dst = static_cast<__half *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + n0;
 #pragma unroll 1
       for (int c = 0; c < FW; c += 32) {
         uint32_t g[32], u[32];
@@ -319,9 +376,13 @@ struct ExpertGemmTMFP4 {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float g0 = __uint_as_float(g[2 * j]) * ga, g1 = __uint_as_float(g[2 * j + 1]) * ga;
-            const float h0 = g0 / (1.0f + __expf(-g0)) * (__uint_as_float(u[2 * j]) * gb);
-            const float h1 = g1 / (1.0f + __expf(-g1)) * (__uint_as_float(u[2 * j + 1]) * gb);
+            const int n = n0 + c + 2 * j;
+            const float g0 = __uint_as_float(g[2 * j]) * weight_scale(p.g0, p.scale_rows, t.e, n);
+            const float g1 = __uint_as_float(g[2 * j + 1]) * weight_scale(p.g0, p.scale_rows, t.e, n + 1);
+            const float h0 = g0 / (1.0f + __expf(-g0)) *
+                             (__uint_as_float(u[2 * j]) * weight_scale(p.g1, p.scale_rows, t.e, n));
+            const float h1 = g1 / (1.0f + __expf(-g1)) *
+                             (__uint_as_float(u[2 * j + 1]) * weight_scale(p.g1, p.scale_rows, t.e, n + 1));
             pk[j] = pack_f16x2(h0, h1);
           }
           uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
@@ -330,9 +391,9 @@ struct ExpertGemmTMFP4 {
         }
       }
     } else {
-      const float w = valid ? __ldg(p.topk_w + __ldg(p.row_src + t.row0 + row)) * ga : 0.f;
+      const float w = valid ? __ldg(p.topk_w + __ldg(p.row_src + t.row0 + row)) : 0.f;
       __nv_bfloat16 *dst =
-          static_cast<__nv_bfloat16 *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + t.f * FW;
+          static_cast<__nv_bfloat16 *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + n0;
 #pragma unroll 1
       for (int c = 0; c < FW; c += 32) {
         uint32_t a[32];
@@ -341,8 +402,12 @@ struct ExpertGemmTMFP4 {
         if (valid) {
           uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2_(__uint_as_float(a[2 * j]) * w, __uint_as_float(a[2 * j + 1]) * w);
+          for (int j = 0; j < 16; ++j) {
+            const int n = n0 + c + 2 * j;
+            pk[j] = pack_bf16x2_(__uint_as_float(a[2 * j]) * w * weight_scale(p.g0, p.scale_rows, t.e, n),
+                                 __uint_as_float(a[2 * j + 1]) * w *
+                                     weight_scale(p.g0, p.scale_rows, t.e, n + 1));
+          }
           uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
           for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -373,9 +438,18 @@ bool make_act_map(CUtensorMap *m, const void *base, int K, long rows, int box_ro
   return make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, K, rows, 64, box_rows, true);
 }
 
-// packed codes [rows, K/2] and scales [rows, K/16] of one weight tensor
+// Raw-weight tensor maps of one weight tensor [rows, K]: NVFP4 codes [rows, K/2]
+// and scales [rows, K/16]; FP8 codes [rows, K] (no scale map: row scales are
+// read by the epilogue).
+template <class Fmt>
 bool make_weight_maps(CUtensorMap *q, CUtensorMap *s, const void *qp, const void *sp, int K,
                       long rows, int box_rows) {
+  if (Fmt::kPerRowScale) {
+    const bool ok = make_tmap_2d(q, qp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, rows, kFp8RowBytes,
+                                 box_rows, false);
+    *s = *q;
+    return ok;
+  }
   return make_tmap_2d(q, qp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows, kPackedRowBytes,
                       box_rows, false) &&
          make_tmap_2d(s, sp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 16, rows, kScaleBoxBytes,
@@ -393,10 +467,10 @@ Fp4Params base_params(const moe_dims &d, const int32_t *offsets, const int32_t *
   return prm;
 }
 
-template <int BN>
-moe_status launch_fp4_small(const moe_dims &d, const moe_experts &ex, const void *x16,
-                            const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                            void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+template <class Fmt, int BN>
+moe_status launch_packed_small(const moe_dims &d, const moe_experts &ex, const void *x16,
+                               const int32_t *offsets, const int32_t *row_src, const float *topk_w,
+                               void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
   const long Tk = (long)d.T * d.top_k;
   const long max_tt = Tk / BN + std::min<long>(d.E, Tk);
   const int sms = device_sm_count();
@@ -404,56 +478,60 @@ moe_status launch_fp4_small(const moe_dims &d, const moe_experts &ex, const void
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.I;
     if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, BN) ||
-        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_gate, ex.s_gate, d.H, rows, kTileM) ||
-        !make_weight_maps(&prm.tmap_q1, &prm.tmap_s1, ex.w_up, ex.s_up, d.H, rows, kTileM))
+        !make_weight_maps<Fmt>(&prm.tmap_q0, &prm.tmap_s0, ex.w_gate, ex.s_gate, d.H, rows, kTileM) ||
+        !make_weight_maps<Fmt>(&prm.tmap_q1, &prm.tmap_s1, ex.w_up, ex.s_up, d.H, rows, kTileM))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_gate;
     prm.g1 = ex.g_up;
+    prm.scale_rows = Fmt::kPerRowScale ? d.I : 0;
     prm.out = h16;
     prm.out_cols = d.I;
     prm.w_rows = d.I;
     prm.ksteps = d.H / kTileK;
     prm.mt = d.I / kTileM;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
-    const moe_status st = launch_fp4<ExpertGemmFP4<BN, true>>(prm, grid, stream);
+    const moe_status st = launch_fp4<ExpertGemmFP4<Fmt, BN, true>>(prm, grid, stream);
     if (st != MOE_OK) return st;
   }
   {
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.H;
     if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, BN) ||
-        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_down, ex.s_down, d.I, rows, kTileM))
+        !make_weight_maps<Fmt>(&prm.tmap_q0, &prm.tmap_s0, ex.w_down, ex.s_down, d.I, rows, kTileM))
       return MOE_ERR_CUDA;
     prm.tmap_q1 = prm.tmap_q0;
     prm.tmap_s1 = prm.tmap_s0;
     prm.g0 = ex.g_down;
     prm.g1 = ex.g_down;
+    prm.scale_rows = Fmt::kPerRowScale ? d.H : 0;
     prm.out = y_partial;
     prm.out_cols = d.H;
     prm.w_rows = d.H;
     prm.ksteps = d.I / kTileK;
     prm.mt = d.H / kTileM;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
-    return launch_fp4<ExpertGemmFP4<BN, false>>(prm, grid, stream);
+    return launch_fp4<ExpertGemmFP4<Fmt, BN, false>>(prm, grid, stream);
   }
 }
 
-moe_status launch_fp4_large(const moe_dims &d, const moe_experts &ex, const void *x16,
-                            const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                            void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+template <class Fmt>
+moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const void *x16,
+                               const int32_t *offsets, const int32_t *row_src, const float *topk_w,
+                               void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
   const long Tk = (long)d.T * d.top_k;
   const long max_tt = Tk / kTileM + std::min<long>(d.E, Tk);
   const int sms = device_sm_count();
   {
-    using P = ExpertGemmTMFP4<true>;
+    using P = ExpertGemmTMFP4<Fmt, true>;
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.I;
     if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, kTileM) ||
-        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_gate, ex.s_gate, d.H, rows, 128) ||
-        !make_weight_maps(&prm.tmap_q1, &prm.tmap_s1, ex.w_up, ex.s_up, d.H, rows, 128))
+        !make_weight_maps<Fmt>(&prm.tmap_q0, &prm.tmap_s0, ex.w_gate, ex.s_gate, d.H, rows, 128) ||
+        !make_weight_maps<Fmt>(&prm.tmap_q1, &prm.tmap_s1, ex.w_up, ex.s_up, d.H, rows, 128))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_gate;
     prm.g1 = ex.g_up;
+    prm.scale_rows = Fmt::kPerRowScale ? d.I : 0;
     prm.out = h16;
     prm.out_cols = d.I;
     prm.w_rows = d.I;
@@ -464,16 +542,17 @@ moe_status launch_fp4_large(const moe_dims &d, const moe_experts &ex, const void
     if (st != MOE_OK) return st;
   }
   {
-    using P = ExpertGemmTMFP4<false>;
+    using P = ExpertGemmTMFP4<Fmt, false>;
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.H;
     if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, kTileM) ||
-        !make_weight_maps(&prm.tmap_q0, &prm.tmap_s0, ex.w_down, ex.s_down, d.I, rows, 256))
+        !make_weight_maps<Fmt>(&prm.tmap_q0, &prm.tmap_s0, ex.w_down, ex.s_down, d.I, rows, 256))
       return MOE_ERR_CUDA;
     prm.tmap_q1 = prm.tmap_q0;
     prm.tmap_s1 = prm.tmap_s0;
     prm.g0 = ex.g_down;
     prm.g1 = ex.g_down;
+    prm.scale_rows = Fmt::kPerRowScale ? d.H : 0;
     prm.out = y_partial;
     prm.out_cols = d.H;
     prm.w_rows = d.H;
@@ -481,6 +560,23 @@ moe_status launch_fp4_large(const moe_dims &d, const moe_experts &ex, const void
     prm.mt = d.H / P::FW;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
     return launch_fp4<P>(prm, grid, stream);
+  }
+}
+
+template <class Fmt>
+moe_status launch_packed(const moe_dims &d, const moe_experts &ex, const void *x16,
+                         const int32_t *offsets, const int32_t *row_src, const float *topk_w,
+                         void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+  const long mean_rows = ((long)d.T * d.top_k + d.E - 1) / d.E;
+  if (mean_rows >= 128 && d.H % 256 == 0)
+    return launch_packed_large<Fmt>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status,
+                                    stream);
+  switch (expert_bn(d)) {
+    case 16: return launch_packed_small<Fmt, 16>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 32: return launch_packed_small<Fmt, 32>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 64: return launch_packed_small<Fmt, 64>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 128: return launch_packed_small<Fmt, 128>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
+    default: return launch_packed_small<Fmt, 256>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
   }
 }
 
@@ -506,17 +602,11 @@ moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const vo
                               const int32_t *expert_offsets, const int32_t *row_src,
                               const float *topk_w, void *y_partial, void *h16, uint32_t *status,
                               cudaStream_t stream) {
-  const long mean_rows = ((long)d.T * d.top_k + d.E - 1) / d.E;
-  if (mean_rows >= 128 && d.H % 256 == 0)
-    return launch_fp4_large(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status,
-                            stream);
-  switch (expert_bn(d)) {
-    case 16: return launch_fp4_small<16>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
-    case 32: return launch_fp4_small<32>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
-    case 64: return launch_fp4_small<64>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
-    case 128: return launch_fp4_small<128>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
-    default: return launch_fp4_small<256>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16, status, stream);
-  }
+  if (ex.dtype == MOE_W_FP8)
+    return launch_packed<Fp8Format>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16,
+                                    status, stream);
+  return launch_packed<Nvfp4Format>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial, h16,
+                                    status, stream);
 }
 
 }  // namespace beam

@@ -95,7 +95,7 @@ inline WsLayout ws_layout(const moe_dims &d, moe_op op, moe_wdtype wdtype = MOE_
     L.x_perm = take(Tk * d.H * 2);
   }
   if (op == MOE_OP_EXPERTS || fwd) L.h = take(Tk * d.I * 2);
-  if (op == MOE_OP_EXPERTS && wdtype == MOE_W_NVFP4) L.x16 = take(Tk * d.H * 2);
+  if (op == MOE_OP_EXPERTS && wdtype != MOE_W_BF16) L.x16 = take(Tk * d.H * 2);
   if (fwd) L.y_partial = take(Tk * d.H * 2);
   L.total = off;
   return L;
@@ -132,7 +132,7 @@ moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *
                           const float *topk_w, void *y_partial, __nv_bfloat16 *h,
                           uint32_t *status, cudaStream_t stream);
 
-// NVFP4 expert weights: x16 and h16 are f16 [Tk, H] and [Tk, I].
+// NVFP4 or FP8 expert weights: x16 and h16 are f16 [Tk, H] and [Tk, I].
 moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const void *x16,
                               const int32_t *expert_offsets, const int32_t *row_src,
                               const float *topk_w, void *y_partial, void *h16, uint32_t *status,

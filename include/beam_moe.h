@@ -56,7 +56,11 @@
  *                  low nibble, s_* e4m3 uint8 [E, N, K/16] (one scale per 16
  *                  consecutive k), g_* fp32 [E] global scales; the weight is
  *                  e2m1 * e4m3 * global.  (N, K) = (I, H) for gate and up,
- *                  (H, I) for down.
+ *                  (H, I) for down.  Needs H % 256 == 0 and I % 256 == 0.
+ *   FP8 experts:   w_* e4m3 uint8 [E, N, K]; g_* fp32 [E, N], one scale per
+ *                  output row (the pages give no FP8 layout: this is the plain
+ *                  reading that keeps dequantisation exact); s_* unused.
+ *                  The weight is e4m3 * g[e, n].
  */
 #ifndef BEAM_MOE_H
 #define BEAM_MOE_H
@@ -80,7 +84,7 @@ typedef enum {
   MOE_ERR_NOT_IMPLEMENTED = 6
 } moe_status;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wdtype;
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_FP8 = 2 } moe_wdtype;
 
 /* Which entry point a workspace is sized for. */
 typedef enum {
@@ -107,9 +111,10 @@ typedef struct {
 
 typedef struct {
   moe_wdtype dtype;
-  const void *w_gate, *w_up, *w_down;    /* bf16, or packed e2m1 (NVFP4)  */
-  const uint8_t *s_gate, *s_up, *s_down; /* e4m3 block scales (NVFP4 only) */
-  const float *g_gate, *g_up, *g_down;   /* fp32 [E] global (NVFP4 only)   */
+  const void *w_gate, *w_up, *w_down;    /* bf16, packed e2m1 (NVFP4) or e4m3 (FP8) */
+  const uint8_t *s_gate, *s_up, *s_down; /* e4m3 block scales (NVFP4 only)          */
+  const float *g_gate, *g_up, *g_down;   /* fp32 [E] globals (NVFP4), [E, N] row
+                                            scales (FP8)                            */
 } moe_experts;
 
 /* Library version, major * 10000 + minor * 100 + patch. */

@@ -42,7 +42,7 @@ class MoeConfig:
     I: int
     routed_scale: float = 2.5
     bias: str = "normal"        # "normal" N(0, 0.01) | "zero" | "zipf"
-    weights: str = "bf16"       # "bf16" | "nvfp4"
+    weights: str = "bf16"       # "bf16" | "nvfp4" | "fp8"
     zipf_alpha: float = 0.0     # scale of log(Zipf) bias for bias="zipf"
 
     def with_T(self, T: int) -> "MoeConfig":
@@ -67,6 +67,7 @@ CONFIGS = {
     "prefill": MoeConfig("prefill", T=16384, bias="zero", **BEAM),
     "skewed": MoeConfig("skewed", T=16384, bias="zipf", zipf_alpha=SKEW_ALPHA, **BEAM),
     "nvfp4": MoeConfig("nvfp4", T=64, weights="nvfp4", **BEAM),
+    "fp8": MoeConfig("fp8", T=64, weights="fp8", **BEAM),
 }
 NVFP4_TOKENS = (1, 64, 1024, 16384)
 
@@ -180,6 +181,29 @@ def quantize_experts_nvfp4(w: torch.Tensor):
     for e in range(E):
         q[e], s[e], g[e] = quantize_nvfp4(w[e])
     return q, s, g
+
+
+# ---------------------------------------------------------------- FP8 packing (data preparation)
+
+
+def quantize_fp8_rows(w: torch.Tensor):
+    """One weight matrix [N, K] -> e4m3 codes uint8 [N, K] and one fp32 scale per
+    row: scale = amax_row / 448, code = e4m3(w / scale) (round to nearest even)."""
+    wf = w.to(torch.float32)
+    amax = wf.abs().amax(dim=1).clamp_min(torch.finfo(torch.float32).tiny)
+    scale = (amax / 448.0).to(torch.float32)
+    q = (wf / scale[:, None]).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).contiguous(), scale.contiguous()
+
+
+def quantize_experts_fp8(w: torch.Tensor):
+    """[E, N, K] bf16 -> (codes uint8 [E, N, K], row scales fp32 [E, N])."""
+    E, N, K = w.shape
+    q = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((E, N), dtype=torch.float32, device=w.device)
+    for e in range(E):
+        q[e], s[e] = quantize_fp8_rows(w[e])
+    return q, s
 
 
 # ---------------------------------------------------------------- views

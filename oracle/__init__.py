@@ -142,16 +142,26 @@ class Nvfp4Matrix:
     g: float
 
 
+@dataclass
+class Fp8Matrix:
+    """FP8 weight [N, K]: e4m3 codes uint8 [N, K] and one fp32 scale per row [N]."""
+    q: np.ndarray
+    row_scale: np.ndarray
+
+
 def _mat_args(m):
     if isinstance(m, Nvfp4Matrix):
         return 1, _c(m.q, np.uint8), _c(m.s, np.uint8), float(m.g)
+    if isinstance(m, Fp8Matrix):
+        return 2, _c(m.q, np.uint8), _c(m.row_scale, np.float32), 1.0
     return 0, _c(m, np.uint16), None, 1.0
 
 
 def expert_swiglu(x_rows: np.ndarray, wg, wu, wd) -> np.ndarray:
     """One SwiGLU expert on n rows; returns fp64 [n, H].
 
-    Weights are bf16 bit patterns (uint16 [I,H], [I,H], [H,I]) or ``Nvfp4Matrix``.
+    Weights are bf16 bit patterns (uint16 [I,H], [I,H], [H,I]), ``Nvfp4Matrix`` or
+    ``Fp8Matrix``.
     """
     lib = _load()
     x = _c(x_rows, np.uint16)

@@ -172,12 +172,15 @@ int oracle_route(int T, int H, int E, int n_group, int topk_group, int top_k,
 /* One weight matrix [N, K] (out x in, K contiguous) of one expert.
  * dtype 0: bf16, data is uint16 [N, K].
  * dtype 1: NVFP4, data is uint8 [N, K/2] (low nibble = even k), scales is
- *          e4m3 uint8 [N, K/16], and the value is e2m1 * e4m3 * global. */
+ *          e4m3 uint8 [N, K/16], and the value is e2m1 * e4m3 * global.
+ * dtype 2: FP8, data is e4m3 uint8 [N, K], row_scale is fp32 [N], and the
+ *          value is e4m3 * row_scale[n] (one scale per output row). */
 typedef struct {
   int dtype;
   const void *data;
   const uint8_t *scales;
   double global;
+  const float *row_scale; /* FP8 only */
   double e2m1[16];  /* value of every e2m1 code (NVFP4 only) */
   double e4m3[256]; /* value of every e4m3 code (NVFP4 only) */
 } oracle_matrix;
@@ -188,6 +191,7 @@ static oracle_matrix make_matrix(int dtype, const void *data, const uint8_t *sca
   m.data = data;
   m.scales = scales;
   m.global = global;
+  m.row_scale = (const float *)scales; /* FP8: the scales argument carries fp32 [N] */
   for (int c = 0; c < 16; ++c) m.e2m1[c] = oracle_e2m1_value((uint8_t)c);
   for (int c = 0; c < 256; ++c) m.e4m3[c] = oracle_e4m3_value((uint8_t)c);
   return m;
@@ -197,6 +201,10 @@ static void decode_row(const oracle_matrix *m, int K, int row, double *out) {
   if (m->dtype == 0) {
     const uint16_t *r = (const uint16_t *)m->data + (size_t)row * K;
     for (int k = 0; k < K; ++k) out[k] = bf16_value(r[k]);
+  } else if (m->dtype == 2) {
+    const uint8_t *q = (const uint8_t *)m->data + (size_t)row * K;
+    const double rs = (double)m->row_scale[row];
+    for (int k = 0; k < K; ++k) out[k] = m->e4m3[q[k]] * rs;
   } else {
     const uint8_t *q = (const uint8_t *)m->data + (size_t)row * (K / 2);
     const uint8_t *sc = m->scales + (size_t)row * (K / 16);

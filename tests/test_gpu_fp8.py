@@ -1,0 +1,78 @@
+"""GPU parity with FP8 expert weights (e4m3 codes with one fp32 scale per
+output row), through the C ABI, against the oracle on the same bytes.  The
+GPU dequantises exactly (e4m3 is exact in f16; the row scale multiplies the
+fp32 accumulator), so the bf16 bars apply."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from parity import compare_routing, output_errors, reference_routing
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import group_limited_routing_bias_b300 as m
+    return m
+
+
+class Fp8Case:
+    def __init__(self, cfg, T=None, seed=0):
+        self.cfg = cfg if T is None else cfg.with_T(T)
+        c = self.cfg
+        x, wr, b = mi.make_router_inputs(c, seed=seed)
+        self.x_h, self.wr_h, self.b_h = x, wr, b
+        self.x, self.wr, self.b = x.to(DEV), wr.to(DEV), b.to(DEV)
+        packed = [mi.quantize_experts_fp8(w) for w in mi.make_expert_weights(c, device=DEV, seed=seed)]
+        (self.qg, self.rg), (self.qu, self.ru), (self.qd, self.rd) = packed
+        torch.cuda.empty_cache()
+
+    def experts(self, lib):
+        return lib.Experts(self.qg, self.qu, self.qd, None, None, None, self.rg, self.ru, self.rd)
+
+    def get_expert(self, e):
+        M = oracle.Fp8Matrix
+        return (M(self.qg[e].cpu().numpy(), self.rg[e].cpu().numpy()),
+                M(self.qu[e].cpu().numpy(), self.ru[e].cpu().numpy()),
+                M(self.qd[e].cpu().numpy(), self.rd[e].cpu().numpy()))
+
+
+def check(lib, case, sample=None):
+    c = case.cfg
+    d = lib.dims_of(c)
+    ws = lib.alloc_workspace(d, lib.MOE_OP_FORWARD, lib.MOE_W_FP8)
+    y = torch.empty(c.T, c.H, dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(c.T, c.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(c.T, c.top_k, dtype=torch.float32, device=DEV)
+    lib.moe_forward(d, case.x, case.wr, case.b, case.experts(lib), y, ws, idx, w)
+    assert lib.workspace_status(ws) == 0
+    idx, w = idx.cpu().numpy(), w.cpu().numpy()
+    orc = oracle.route(mi.bf16_bits(case.x_h), case.wr_h.numpy(), case.b_h.numpy(), c.n_group,
+                       c.topk_group, c.top_k, c.routed_scale, details=True)
+    rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
+    assert rep.ok, (rep, rep.mismatch_info)
+    ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
+    tokens = np.arange(c.T) if sample is None else np.asarray(sample)
+    y_ref = oracle.experts_forward(mi.bf16_bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
+    err = output_errors(y.double().cpu().numpy()[tokens], y_ref)
+    print(f"\n[{c.name} T={c.T}] routing {rep}; output {err} over {len(tokens)} tokens")
+    assert err.ok(), err
+    return y
+
+
+@pytest.mark.parametrize("T", [64, 1, 300, 2048])
+def test_fp8_tiny(lib, T):
+    """T=2048 takes the token-major GEMMs (256 rows per expert on average)."""
+    check(lib, Fp8Case(mi.CONFIGS["tiny"], T=T))
+
+
+@pytest.mark.parametrize("T,n_sample", [(64, None), (16384, 48)])
+def test_fp8_beam(lib, T, n_sample):
+    case = Fp8Case(mi.CONFIGS["fp8"], T=T)
+    sample = None if n_sample is None else np.sort(
+        np.random.default_rng(T).choice(T, n_sample, replace=False))
+    check(lib, case, sample)

@@ -195,3 +195,30 @@ def test_nvfp4_expert_equals_bf16_path_on_decoded_weights(oracle_mod):
     # quantisation error of the packed weights is a few percent of their size
     rel = np.linalg.norm(dg - wg[2].double().numpy()) / np.linalg.norm(wg[2].double().numpy())
     assert rel < 0.12
+
+
+# ------------------------------------------------------------------ FP8 (one scale per row)
+
+
+def test_fp8_matrix_decoding(oracle_mod):
+    """Hand-built FP8 matrix: value = e4m3(code) * row scale."""
+    q = np.array([[56, 64, 1, 184], [126, 0, 57, 63]], np.uint8)  # 1, 2, 2^-9, -1 | 448, 0, 1.125, 1.875
+    rs = np.array([0.5, 3.0], np.float32)
+    dec = oracle_mod.decode_matrix(oracle_mod.Fp8Matrix(q, rs))
+    np.testing.assert_array_equal(dec, [[0.5, 1.0, 2.0 ** -10, -0.5], [1344.0, 0.0, 3.375, 5.625]])
+
+
+def test_fp8_expert_equals_library_matmul_on_decoded_weights(oracle_mod):
+    cfg = mi.CONFIGS["tiny"]
+    wg, wu, wd = mi.make_expert_weights(cfg, seed=6)
+    mats = [oracle_mod.Fp8Matrix(*[t.numpy() for t in mi.quantize_fp8_rows(w[1])])
+            for w in (wg, wu, wd)]
+    x, _, _ = mi.make_router_inputs(cfg, seed=6, T=5)
+    o = oracle_mod.expert_swiglu(mi.bf16_bits(x), *mats)
+    dg, du, dd = [oracle_mod.decode_matrix(m) for m in mats]
+    xd = x.double().numpy()
+    ref = (silu(xd @ dg.T) * (xd @ du.T)) @ dd.T
+    np.testing.assert_allclose(o, ref, rtol=1e-11, atol=1e-12)
+    # e4m3 with a per-row scale keeps about 2^-4 relative error per weight
+    rel = np.linalg.norm(dg - wg[1].double().numpy()) / np.linalg.norm(wg[1].double().numpy())
+    assert rel < 0.05
