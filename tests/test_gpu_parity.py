@@ -289,3 +289,32 @@ def test_empty_batch(lib):
     b = torch.zeros(c.E, device=DEV)
     lib.moe_forward(d, x, wr, b, lib.Experts(wg, wu, wd), y, ws)
     assert lib.workspace_status(ws) == 0
+
+
+# ------------------------------------------------------------------ general router shapes
+
+
+@pytest.mark.parametrize("E,G,kg,k", [
+    (256, 4, 2, 8),     # groups of 64: two slots per lane merged
+    (256, 2, 1, 8),     # groups of 128
+    (256, 1, 1, 8),     # one group of 256: plain top-k
+    (256, 8, 8, 8),     # every group kept
+    (64, 8, 3, 6),      # groups of 8
+    (128, 16, 5, 16),   # 16 groups of 8, top_k 16
+    (32, 16, 4, 3),     # groups of 2
+])
+def test_route_general_shapes(lib, E, G, kg, k):
+    cfg = mi.MoeConfig(f"route-E{E}-G{G}", T=300, H=512, E=E, n_group=G, topk_group=kg, top_k=k,
+                       I=128)
+    case = Case(cfg, weights=False)
+    idx, w = gpu_route(lib, case)
+    check_routing(case, case.oracle_route(), idx, w)
+
+
+@pytest.mark.parametrize("E,G,kg,k,H,I,T", [(64, 4, 2, 6, 384, 384, 700),
+                                             (128, 8, 4, 8, 256, 640, 900)])
+def test_forward_other_shapes(lib, E, G, kg, k, H, I, T):
+    """Forward at shapes other than Beam's (H, I multiples of 128 only)."""
+    cfg = mi.MoeConfig(f"shape-E{E}-H{H}-I{I}", T=T, H=H, E=E, n_group=G, topk_group=kg, top_k=k,
+                       I=I)
+    check_forward(lib, Case(cfg))
