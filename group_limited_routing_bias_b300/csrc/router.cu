@@ -114,40 +114,46 @@ __device__ __forceinline__ void top2_merge(float &a1, float &a2, float b1, float
   a2 = lo;
 }
 
-// One CTA per kTopkTokens tokens.  First all 256 threads add the K-split
-// partial logits of the CTA's tokens, every load issued at once (splits added
-// in split order), into shared memory; then one warp per token does the
-// selection.  Lane l holds experts e = l + 32 i, i = 0..7.
-constexpr int kTopkTokens = 8;
-
+// One CTA per TPB tokens.  First all 256 threads add the K-split partial
+// logits of the CTA's tokens into shared memory, splits added in split order;
+// every load is issued unconditionally from a clamped address (a split past
+// ksplit adds exactly +0.0), so all of a thread's loads are in flight at once.
+// Then one warp per token does the selection.  Lane l holds experts
+// e = l + 32 i, i = 0..7.  With a K split (small T) each CTA takes one token,
+// so a thread waits on one round trip for its kMaxRouterSplit loads.
+template <int TPB>
 __global__ void __launch_bounds__(256) router_topk_kernel(TopkArgs a) {
   constexpr int NS = 8;
-  __shared__ float logits_s[kTopkTokens][256];
+  __shared__ float logits_s[TPB][256];
   const int lane = threadIdx.x & 31;
   const int gsize = 1 << a.log2_gsize;
-  const int t0 = blockIdx.x * kTopkTokens;
+  const int t0 = blockIdx.x * TPB;
   {
     const int e = threadIdx.x;  // blockDim.x == 256 >= E
-    float acc[kTopkTokens];
+    float acc[TPB];
 #pragma unroll
-    for (int j = 0; j < kTopkTokens; ++j) acc[j] = 0.f;
+    for (int j = 0; j < TPB; ++j) acc[j] = 0.f;
     if (e < a.E) {
+      if constexpr (TPB == 1) {
+        float v[kMaxRouterSplit];
 #pragma unroll
-      for (int sp = 0; sp < kMaxRouterSplit; ++sp) {
-        if (sp < a.ksplit) {
-          float v[kTopkTokens];
-#pragma unroll
-          for (int j = 0; j < kTopkTokens; ++j)
-            v[j] = (t0 + j < a.T) ? __ldg(a.partial + ((size_t)sp * a.T + t0 + j) * a.E + e) : 0.f;
-#pragma unroll
-          for (int j = 0; j < kTopkTokens; ++j) acc[j] += v[j];
+        for (int sp = 0; sp < kMaxRouterSplit; ++sp) {
+          const int spc = sp < a.ksplit ? sp : a.ksplit - 1;
+          v[sp] = __ldg(a.partial + ((size_t)spc * a.T + t0) * a.E + e);
         }
+#pragma unroll
+        for (int sp = 0; sp < kMaxRouterSplit; ++sp) acc[0] += sp < a.ksplit ? v[sp] : 0.f;
+      } else {  // TPB > 1 is only launched without a K split
+#pragma unroll
+        for (int j = 0; j < TPB; ++j)
+          acc[j] = __ldg(a.partial + (size_t)min(t0 + j, a.T - 1) * a.E + e);
       }
     }
 #pragma unroll
-    for (int j = 0; j < kTopkTokens; ++j) logits_s[j][e] = acc[j];
+    for (int j = 0; j < TPB; ++j) logits_s[j][e] = acc[j];
   }
   __syncthreads();
+  if ((threadIdx.x >> 5) >= TPB) return;
   const int t = t0 + (threadIdx.x >> 5);
   if (t < a.T) {
     float s[NS], sb[NS];
@@ -320,7 +326,10 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
   a.ksplit = rp.ksplit;
   a.log2_gsize = ilog2(d.E / d.n_group);
   a.routed_scale = d.routed_scale;
-  router_topk_kernel<<<(d.T + kTopkTokens - 1) / kTopkTokens, 256, 0, stream>>>(a);
+  if (rp.ksplit > 1)
+    router_topk_kernel<1><<<d.T, 256, 0, stream>>>(a);
+  else
+    router_topk_kernel<8><<<(d.T + 7) / 8, 256, 0, stream>>>(a);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
