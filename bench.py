@@ -410,6 +410,14 @@ def run_profile(args):
                       "ms_per_step": statistics.mean(per)}))
 
 
+def launches_per_forward(T: int, top_k: int) -> int:
+    """Kernels one moe_forward launches: router (weight split, logits GEMM,
+    top-k), dispatch (one fused kernel when T*k fits one 4096-entry chunk,
+    else count/scan/scatter), row gather, the two expert GEMMs, combine."""
+    dispatch = 1 if T * top_k <= 4096 else 3
+    return 3 + dispatch + 1 + 2 + 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,7 +547,7 @@ def main():
                    "T": cfg.T, "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": 10 * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4, "fp8": fp8,
+        "gpu_launches": launches_per_forward(cfg.T, cfg.top_k) * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4, "fp8": fp8,
     }
     print(json.dumps(line))
     if dist is not None:

@@ -4,6 +4,7 @@
 // expert (a stable counting sort).  Then the x rows are gathered into that
 // order so each expert's rows are contiguous for the grouped GEMMs.
 //
+//   permute_small_kernel   one CTA, when T*k fits one chunk: all three steps below
 //   permute_count_kernel   one CTA per chunk of 4096 entries: histogram
 //   permute_scan_kernel    one CTA: per-chunk bases and expert offsets
 //   permute_scatter_kernel one CTA per chunk: warp-ordered ranks -> slots
@@ -134,6 +135,67 @@ __global__ void __launch_bounds__(kChunkThreads)
   }
 }
 
+// All of count, scan and scatter in one CTA, for batches of at most one chunk
+// (T*k <= 4096 entries, e.g. decode): per-warp counts in entry order, per
+// expert totals and their exclusive scan, then the same warp-ordered slots as
+// the multi-CTA path.
+__global__ void __launch_bounds__(kChunkThreads)
+    permute_small_kernel(const int32_t *__restrict__ idx, int Tk, int E,
+                         int32_t *__restrict__ offsets, int32_t *__restrict__ slot_of,
+                         int32_t *__restrict__ row_src, uint32_t *status) {
+  extern __shared__ int wcnt[];  // [32 warps][E]
+  __shared__ int warp_sums[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int wbase = warp * kEntriesPerWarp;
+  int *mine = wcnt + warp * E;
+  bool bad = false;
+  for (int sub = 0; sub < kEntriesPerWarp; sub += 32) {
+    const int n = wbase + sub + lane;
+    int e = n < Tk ? idx[n] : -1;
+    if (n < Tk && (e < 0 || e >= E)) bad = true;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) atomicOr(status, (uint32_t)MOE_DEV_BAD_INDEX);
+  __syncthreads();
+  // per expert: total over warps, then the exclusive scan over experts
+  int total = 0;
+  if (threadIdx.x < E)
+    for (int w = 0; w < 32; ++w) total += wcnt[w * E + threadIdx.x];
+  const int start = block_exclusive_scan(threadIdx.x < E ? total : 0, warp_sums);
+  if (threadIdx.x < E) {
+    int run = start;
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + threadIdx.x];
+      wcnt[w * E + threadIdx.x] = run;
+      run += c;
+    }
+    offsets[threadIdx.x] = start;
+    if (threadIdx.x == E - 1) offsets[E] = start + total;
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int sub = 0; sub < kEntriesPerWarp; sub += 32) {
+    const int n = wbase + sub + lane;
+    int e = n < Tk ? idx[n] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int slot = -1;
+    if (e >= 0) slot = mine[e] + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+    if (n < Tk) {
+      slot_of[n] = slot;
+      if (slot >= 0) row_src[slot] = n;
+    }
+  }
+}
+
 // Copies x rows into permuted order; with TO_F16 the bf16 values are written
 // as f16 (exact for |v| >= 2^-14; the NVFP4 expert GEMMs run on f16 operands).
 template <bool TO_F16>
@@ -180,11 +242,17 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
       return MOE_ERR_CUDA;
     attr_set = true;
   }
-  permute_count_kernel<<<nchunks, kChunkThreads, d.E * 4, stream>>>(topk_idx, Tk, d.E, counts,
-                                                                     status);
-  permute_scan_kernel<<<1, 256, 0, stream>>>(counts, nchunks, d.E, bases, expert_offsets);
-  permute_scatter_kernel<<<nchunks, kChunkThreads, scatter_smem, stream>>>(topk_idx, Tk, d.E, bases,
-                                                                          slot_of, row_src);
+  if (nchunks == 1) {
+    permute_small_kernel<<<1, kChunkThreads, scatter_smem, stream>>>(topk_idx, Tk, d.E,
+                                                                     expert_offsets, slot_of,
+                                                                     row_src, status);
+  } else {
+    permute_count_kernel<<<nchunks, kChunkThreads, d.E * 4, stream>>>(topk_idx, Tk, d.E, counts,
+                                                                       status);
+    permute_scan_kernel<<<1, 256, 0, stream>>>(counts, nchunks, d.E, bases, expert_offsets);
+    permute_scatter_kernel<<<nchunks, kChunkThreads, scatter_smem, stream>>>(
+        topk_idx, Tk, d.E, bases, slot_of, row_src);
+  }
   if (Tk > 0) {
     const int blocks = std::max(1, std::min((Tk + 7) / 8, device_sm_count() * 8));
     if (f16_out)

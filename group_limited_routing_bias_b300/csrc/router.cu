@@ -17,22 +17,39 @@
 
 namespace beam {
 
-__global__ void router_split_kernel(const float *__restrict__ w, __nv_bfloat16 *__restrict__ w3,
-                                    int E, int H) {
-  const size_t n = (size_t)E * H;
+// Eight consecutive weights per thread: two 16-byte loads, three 16-byte stores.
+__global__ void router_split_kernel(const float4 *__restrict__ w, uint4 *__restrict__ w3, int E,
+                                    int H) {
+  const int vec_per_row = H / 8;
+  const size_t n = (size_t)E * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
-    const int e = (int)(i / H), h = (int)(i % H);
-    const float v = w[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(hi);  // exact: v and hi share the top bits
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);  // exact, at most 8 significant bits
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-    __nv_bfloat16 *row = w3 + (size_t)e * 3 * H;
-    row[h] = hi;
-    row[H + h] = mid;
-    row[2 * H + h] = lo;
+    const int e = (int)(i / vec_per_row), v = (int)(i % vec_per_row);
+    const float4 a = w[2 * i], b = w[2 * i + 1];
+    const float src[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float r0[2], r1[2], r2[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float x = src[2 * j + q];
+        r0[q] = __bfloat162float(__float2bfloat16_rn(x));
+        const float d1 = x - r0[q];  // exact: x and its bf16 rounding share the top bits
+        r1[q] = __bfloat162float(__float2bfloat16_rn(d1));
+        r2[q] = d1 - r1[q];  // exact, at most 8 significant bits, so exact in bf16
+      }
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(r0[0], r0[1]);
+      const __nv_bfloat162 m2 = __floats2bfloat162_rn(r1[0], r1[1]);
+      const __nv_bfloat162 l2 = __floats2bfloat162_rn(r2[0], r2[1]);
+      hi[j] = *reinterpret_cast<const uint32_t *>(&h2);
+      mid[j] = *reinterpret_cast<const uint32_t *>(&m2);
+      lo[j] = *reinterpret_cast<const uint32_t *>(&l2);
+    }
+    uint4 *row = w3 + (size_t)e * 3 * vec_per_row;
+    row[v] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    row[vec_per_row + v] = make_uint4(mid[0], mid[1], mid[2], mid[3]);
+    row[2 * vec_per_row + v] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -301,9 +318,10 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
                         int32_t *topk_idx, float *topk_w, const RouterPlan &rp,
                         __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream) {
   {
-    const size_t n = (size_t)d.E * d.H;
+    const size_t n = (size_t)d.E * d.H / 8;
     const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
-    router_split_kernel<<<blocks, 256, 0, stream>>>(w_router, w3, d.E, d.H);
+    router_split_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(w_router),
+                                                    reinterpret_cast<uint4 *>(w3), d.E, d.H);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   moe_status st;
