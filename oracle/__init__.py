@@ -66,6 +66,14 @@ def _load():
     lib.oracle_bias_update.restype = f
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = d
+    lib.oracle_e2m1_rne.argtypes = [f]
+    lib.oracle_e2m1_rne.restype = ctypes.c_uint8
+    lib.oracle_e4m3_rne.argtypes = [f]
+    lib.oracle_e4m3_rne.restype = ctypes.c_uint8
+    lib.oracle_quantize_nvfp4.argtypes = [i, i, P, f, P, P]
+    lib.oracle_quantize_nvfp4.restype = i
+    lib.oracle_expert_swiglu_w4a4.argtypes = [i, i, i, P, P, P, d, P, P, d, P, P, d, f, f, P]
+    lib.oracle_expert_swiglu_w4a4.restype = i
     _lib = lib
     return lib
 
@@ -211,16 +219,59 @@ def e4m3_value(code: int) -> float:
     return _load().oracle_e4m3_value(code)
 
 
+def e2m1_rne(v: float) -> int:
+    """fp32 -> E2M1 code (round to nearest, ties to even mantissa, saturate at 6)."""
+    return _load().oracle_e2m1_rne(v)
+
+
+def e4m3_rne(v: float) -> int:
+    """fp32 -> E4M3 code (round to nearest, ties to even, saturate at 448)."""
+    return _load().oracle_e4m3_rne(v)
+
+
+def quantize_nvfp4(v: np.ndarray, g: float):
+    """NVFP4 activation quantiser (readings in moe_oracle.c): fp32 [rows, cols]
+    and a global scale -> (codes uint8 [rows, cols/2], scales uint8 [rows, cols/16])."""
+    lib = _load()
+    a = _c(v, np.float32)
+    rows, cols = a.shape
+    q = np.empty((rows, cols // 2), np.uint8)
+    sc = np.empty((rows, cols // 16), np.uint8)
+    if lib.oracle_quantize_nvfp4(rows, cols, _ptr(a), g, _ptr(q), _ptr(sc)) != 0:
+        raise ValueError("oracle_quantize_nvfp4: bad arguments")
+    return q, sc
+
+
+def expert_swiglu_w4a4(x_rows: np.ndarray, wg: Nvfp4Matrix, wu: Nvfp4Matrix, wd: Nvfp4Matrix,
+                       gx: float, gh: float) -> np.ndarray:
+    """One SwiGLU expert with NVFP4 weights and NVFP4 activations (x quantised
+    with global gx, h with gh); returns fp64 [n, H]."""
+    lib = _load()
+    x = _c(x_rows, np.uint16)
+    n, H = x.shape
+    I = wg.q.shape[0]
+    o = np.empty((n, H), np.float64)
+    args = []
+    for m in (wg, wu, wd):
+        args += [_ptr(_c(m.q, np.uint8)), _ptr(_c(m.s, np.uint8)), float(m.g)]
+    if lib.oracle_expert_swiglu_w4a4(n, H, I, _ptr(x), *args, gx, gh, _ptr(o)) != 0:
+        raise ValueError("oracle_expert_swiglu_w4a4: bad arguments")
+    return o
+
+
 ExpertFn = Callable[[int], tuple]
 
 
 def experts_forward(x_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, get_expert: ExpertFn,
-                    tokens: Optional[Sequence[int]] = None) -> np.ndarray:
+                    tokens: Optional[Sequence[int]] = None,
+                    a4: Optional[tuple] = None) -> np.ndarray:
     """Expert path for a given routing: per-expert SwiGLU, then the combine.
 
     ``get_expert(e)`` returns the three weight matrices of expert e (so large
     weight sets can be fetched one expert at a time).  ``tokens`` restricts
     the outputs to a subset of token indices (rows of the result follow it).
+    ``a4 = (gx, gh)`` selects NVFP4 activations (W4A4) with those global
+    scales; the weights must then be ``Nvfp4Matrix``.
     Returns fp64 [len(tokens), H].
     """
     x = _c(x_bf16, np.uint16)
@@ -232,7 +283,10 @@ def experts_forward(x_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, get_expe
     for e in np.unique(sub_idx):
         rr, kk = np.nonzero(sub_idx == e)
         wg, wu, wd = get_expert(int(e))
-        o[rr, kk] = expert_swiglu(x[sel[rr]], wg, wu, wd)
+        if a4 is None:
+            o[rr, kk] = expert_swiglu(x[sel[rr]], wg, wu, wd)
+        else:
+            o[rr, kk] = expert_swiglu_w4a4(x[sel[rr]], wg, wu, wd, a4[0], a4[1])
     return combine(np.ascontiguousarray(w[sel]), o)
 
 

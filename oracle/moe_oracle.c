@@ -167,6 +167,72 @@ int oracle_route(int T, int H, int E, int n_group, int topk_group, int top_k,
   return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }
 
+/* ---- rounding to the narrow formats (NVFP4 activation quantiser) -------- */
+
+/* fp32 -> FP4 E2M1 code, round to nearest, ties to the code whose mantissa
+ * bit is 0; magnitudes above 6 saturate to 6.  The sign bit is the value's
+ * sign, so a negative value that rounds to zero gives the code of -0. */
+uint8_t oracle_e2m1_rne(float v) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const uint8_t sign = signbit(v) ? 8 : 0;
+  const double a = fabs((double)v);
+  if (a >= 6.0) return sign | 7;
+  int c = 0;
+  while (mag[c + 1] <= a) ++c; /* mag[c] <= a < mag[c+1] */
+  const double dlo = a - mag[c], dhi = mag[c + 1] - a;
+  int code = (dlo < dhi) ? c : (dhi < dlo) ? c + 1 : ((c & 1) ? c + 1 : c);
+  return sign | (uint8_t)code;
+}
+
+/* fp32 -> FP8 E4M3 code, round to nearest, ties to the even code; magnitudes
+ * at or above 448 saturate to 448 (code 0x7E).  Same sign rule as above. */
+uint8_t oracle_e4m3_rne(float v) {
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  int c = 0; /* codes 0..126 are the finite magnitudes in increasing order */
+  while (oracle_e4m3_value((uint8_t)(c + 1)) <= a) ++c;
+  const double lo = oracle_e4m3_value((uint8_t)c), hi = oracle_e4m3_value((uint8_t)(c + 1));
+  const double dlo = a - lo, dhi = hi - a;
+  int code = (dlo < dhi) ? c : (dhi < dlo) ? c + 1 : ((c & 1) ? c + 1 : c);
+  return sign | (uint8_t)code;
+}
+
+/*
+ * NVFP4 quantisation of activations with a given fp32 global scale g > 0
+ * (the reading of "NVFP4" for activations: the weights' two-level format, a
+ * static global scale per tensor and one E4M3 scale per 16 consecutive
+ * values of a row).  For every block of 16 values v of a row, in fp32:
+ *   amax = max |v|,  s = e4m3_rne(amax / (6 * g)),  scale = e4m3(s) * g,
+ *   code_i = e2m1_rne(v_i / scale)            (all codes 0 when scale == 0).
+ * v is fp32 [rows, cols] (cols % 16 == 0); q is uint8 [rows, cols/2] with
+ * the even column in the low nibble; s is uint8 [rows, cols/16].
+ * The value a code stands for is e2m1(code) * e4m3(s) * g.
+ */
+int oracle_quantize_nvfp4(int rows, int cols, const float *v, float g, uint8_t *q, uint8_t *s) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || !(g > 0.0f)) return ORACLE_BAD_ARG;
+  const float six_g = 6.0f * g;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    for (int b = 0; b < cols / 16; ++b) {
+      const float *blk = v + (size_t)r * cols + 16 * b;
+      float amax = 0.0f;
+      for (int i = 0; i < 16; ++i)
+        if (fabsf(blk[i]) > amax) amax = fabsf(blk[i]);
+      const uint8_t sc = oracle_e4m3_rne(amax / six_g);
+      const float scale = (float)oracle_e4m3_value(sc) * g;
+      s[(size_t)r * (cols / 16) + b] = sc;
+      uint8_t *qb = q + (size_t)r * (cols / 2) + 8 * b;
+      for (int i = 0; i < 16; i += 2) {
+        const uint8_t c0 = scale == 0.0f ? 0 : oracle_e2m1_rne(blk[i] / scale);
+        const uint8_t c1 = scale == 0.0f ? 0 : oracle_e2m1_rne(blk[i + 1] / scale);
+        qb[i / 2] = (uint8_t)(c0 | (c1 << 4));
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* ---- expert weights ---------------------------------------------------- */
 
 /* One weight matrix [N, K] (out x in, K contiguous) of one expert.
@@ -281,6 +347,87 @@ int oracle_expert_swiglu(int n, int H, int I, const uint16_t *x,
     free(rd);
   }
   free(xd); free(act);
+  return ORACLE_OK;
+}
+
+/*
+ * The same expert with NVFP4 weights and NVFP4 activations (W4A4):
+ *   x_hat = dequant(quantize(x, gx))                 (x: bf16 rows, exact in fp32)
+ *   g, u  = W_gate . x_hat, W_up . x_hat             (fp64)
+ *   h     = fp32( silu(g) * u )                      (one rounding to fp32)
+ *   h_hat = dequant(quantize(h, gh))
+ *   o     = W_down . h_hat                           (fp64)
+ * with quantize/dequant as in oracle_quantize_nvfp4 (blocks of 16 along H for
+ * x and along I for h).  Weights are NVFP4 as in oracle_matrix (dtype 1).
+ */
+int oracle_expert_swiglu_w4a4(int n, int H, int I, const uint16_t *x,
+                              const void *wg, const uint8_t *sg, double gg,
+                              const void *wu, const uint8_t *su, double gu,
+                              const void *wd, const uint8_t *sd, double gd,
+                              float gx, float gh, double *o) {
+  if (n < 0 || H <= 0 || I <= 0 || H % 16 || I % 16 || !(gx > 0.0f) || !(gh > 0.0f))
+    return ORACLE_BAD_ARG;
+  if (n == 0) return ORACLE_OK;
+  oracle_matrix mg = make_matrix(1, wg, sg, gg), mu = make_matrix(1, wu, su, gu),
+                md = make_matrix(1, wd, sd, gd);
+  float *xf = (float *)malloc(sizeof(float) * (size_t)n * H);
+  float *hf = (float *)malloc(sizeof(float) * (size_t)n * I);
+  uint8_t *xq = (uint8_t *)malloc((size_t)n * H / 2), *xs = (uint8_t *)malloc((size_t)n * H / 16);
+  uint8_t *hq = (uint8_t *)malloc((size_t)n * I / 2), *hs = (uint8_t *)malloc((size_t)n * I / 16);
+  double *xd = (double *)malloc(sizeof(double) * (size_t)n * H);
+  double *hd = (double *)malloc(sizeof(double) * (size_t)n * I);
+  if (!xf || !hf || !xq || !xs || !hq || !hs || !xd || !hd) {
+    free(xf); free(hf); free(xq); free(xs); free(hq); free(hs); free(xd); free(hd);
+    return ORACLE_BAD_ARG;
+  }
+  for (size_t i = 0; i < (size_t)n * H; ++i) xf[i] = (float)bf16_value(x[i]);
+  oracle_quantize_nvfp4(n, H, xf, gx, xq, xs);
+  for (int r = 0; r < n; ++r)
+    for (int h = 0; h < H; ++h) {
+      const uint8_t byte = xq[(size_t)r * (H / 2) + h / 2];
+      const uint8_t code = (h & 1) ? (byte >> 4) : (byte & 15);
+      xd[(size_t)r * H + h] = mg.e2m1[code] * mg.e4m3[xs[(size_t)r * (H / 16) + h / 16]] * (double)gx;
+    }
+#pragma omp parallel
+  {
+    double *rg = (double *)malloc(sizeof(double) * H);
+    double *ru = (double *)malloc(sizeof(double) * H);
+#pragma omp for schedule(static)
+    for (int i = 0; i < I; ++i) {
+      decode_row(&mg, H, i, rg);
+      decode_row(&mu, H, i, ru);
+      for (int r = 0; r < n; ++r) {
+        const double *xr = xd + (size_t)r * H;
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) { g += rg[h] * xr[h]; u += ru[h] * xr[h]; }
+        hf[(size_t)r * I + i] = (float)(g / (1.0 + exp(-g)) * u);
+      }
+    }
+    free(rg); free(ru);
+  }
+  oracle_quantize_nvfp4(n, I, hf, gh, hq, hs);
+  for (int r = 0; r < n; ++r)
+    for (int i = 0; i < I; ++i) {
+      const uint8_t byte = hq[(size_t)r * (I / 2) + i / 2];
+      const uint8_t code = (i & 1) ? (byte >> 4) : (byte & 15);
+      hd[(size_t)r * I + i] = md.e2m1[code] * md.e4m3[hs[(size_t)r * (I / 16) + i / 16]] * (double)gh;
+    }
+#pragma omp parallel
+  {
+    double *rd = (double *)malloc(sizeof(double) * I);
+#pragma omp for schedule(static)
+    for (int j = 0; j < H; ++j) {
+      decode_row(&md, I, j, rd);
+      for (int r = 0; r < n; ++r) {
+        const double *ar = hd + (size_t)r * I;
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += rd[i] * ar[i];
+        o[(size_t)r * H + j] = acc;
+      }
+    }
+    free(rd);
+  }
+  free(xf); free(hf); free(xq); free(xs); free(hq); free(hs); free(xd); free(hd);
   return ORACLE_OK;
 }
 
