@@ -118,14 +118,14 @@ class ClockSampler:
 class Workload:
     """Seeded inputs of one workload resident on the GPU, plus buffers."""
 
-    def __init__(self, lib, cfg, weights, dev, stages=True):
+    def __init__(self, lib, cfg, weights, dev, stages=True, a4=None):
         import moe_inputs as mi
         self.cfg = cfg
         self.d = lib.dims_of(cfg)
         x, wr, b = mi.make_router_inputs(cfg)
         self.x_host = x.pin_memory()
         self.x, self.wr, self.b = x.to(dev), wr.to(dev), b.to(dev)
-        self.experts = lib.Experts(*weights)
+        self.experts = lib.Experts(*weights, a4=a4)
         self.wdtype = self.experts.dtype
         self.ws = lib.alloc_workspace(self.d, lib.MOE_OP_FORWARD, self.wdtype, device=dev)
         T, H, k, E = cfg.T, cfg.H, cfg.top_k, cfg.E
@@ -200,6 +200,7 @@ def e2e_steps(lib, wl, steps, flush):
 
 FP4_EXPERT_BYTES = 3 * (5120 * 2560 // 2 + 5120 * 2560 // 16) + 3 * 4  # codes + e4m3 scales + globals
 FP8_EXPERT_BYTES = 3 * 5120 * 2560 + (2 * 2560 + 5120) * 4              # e4m3 codes + row scales
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate of B300
 
 
 def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
@@ -232,14 +233,15 @@ def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
     return out
 
 
-def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks):
+def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks, a4=None):
     """Packed experts (NVFP4 or FP8): decode T=64 (HBM-bound: packed bytes of
     touched experts) and prefill T=16384 (W4A16 / W8A16: the bf16 tensor peak
-    is its denominator)."""
+    is its denominator; W4A4 (a4 given): the fp4 peak, the measured bf16 peak
+    times the nominal fp4/bf16 ratio 13.5/2.25)."""
     out = {}
     for name, T, steps in (("decode", 64, 50), ("prefill", 16384, 5)):
         cfg = mi.CONFIGS[fmt].with_T(T)
-        wl = Workload(lib, cfg, wts, dev)
+        wl = Workload(lib, cfg, wts, dev, a4=a4)
         for _ in range(3):
             wl.forward(lib)
         torch.cuda.synchronize()
@@ -256,6 +258,10 @@ def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks):
         else:
             tf = T * FLOP_PER_TOKEN / (st["experts"] / 1000.0) / 1e12
             fig.update({"expert_gemm_tflops": tf, "frac_of_bf16_burst_peak": tf / peaks["bf16"]})
+            if a4 is not None:
+                fp4_peak = peaks["bf16"] * FP4_OVER_BF16
+                fig.update({"peak_fp4_tflops": fp4_peak, "frac_of_fp4_peak": tf / fp4_peak,
+                            "peak_fp4_source": "measured bf16 burst x nominal 13.5/2.25"})
         out[name] = fig
         del wl
         torch.cuda.empty_cache()
@@ -382,6 +388,8 @@ def profile_config(name):
              "nvfp4-decode-small": mi.MoeConfig("nvfp4-decode-small", T=64, weights="nvfp4", **small),
              "nvfp4-prefill-small": mi.MoeConfig("nvfp4-prefill-small", T=4096, bias="zero",
                                                  weights="nvfp4", **small)}
+    if name.startswith("w4a4-"):  # the NVFP4 workloads with NVFP4 activations
+        name = "nvfp4-" + name[len("w4a4-"):]
     return extra[name] if name in extra else mi.CONFIGS[name]
 
 
@@ -400,7 +408,8 @@ def run_profile(args):
         packed = [mi.quantize_experts_fp8(w) for w in weights]
         weights = tuple(p[0] for p in packed) + (None, None, None) + tuple(p[1] for p in packed)
         torch.cuda.empty_cache()
-    wl = Workload(lib, cfg, weights, dev, stages=False)
+    a4 = (mi.A4_X_GLOBAL, mi.A4_H_GLOBAL) if args.profile.startswith("w4a4-") else None
+    wl = Workload(lib, cfg, weights, dev, stages=False, a4=a4)
     for _ in range(args.warmup):
         wl.forward(lib)
     torch.cuda.synchronize()
@@ -431,7 +440,8 @@ def main():
     ap.add_argument("--profile", choices=["decode", "prefill", "skewed", "prefill-small",
                                           "decode-small", "nvfp4-decode", "nvfp4-prefill",
                                           "nvfp4-decode-small", "nvfp4-prefill-small",
-                                          "fp8-decode"], default=None,
+                                          "fp8-decode", "w4a4-decode", "w4a4-prefill",
+                                          "w4a4-decode-small", "w4a4-prefill-small"], default=None,
                     help="run only warm-up + steps forwards of one workload (for ncu)")
     args = ap.parse_args()
     peaks = load_peaks()
@@ -526,6 +536,8 @@ def main():
         packed = [mi.quantize_experts_nvfp4(w) for w in weights]
         fp4w = tuple(p[0] for p in packed) + tuple(p[1] for p in packed) + tuple(p[2] for p in packed)
         nvfp4 = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks)
+        nvfp4["w4a4"] = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks,
+                                       a4=(mi.A4_X_GLOBAL, mi.A4_H_GLOBAL))
         del packed, fp4w
         torch.cuda.empty_cache()
         packed = [mi.quantize_experts_fp8(w) for w in weights]

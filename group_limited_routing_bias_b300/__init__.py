@@ -21,14 +21,14 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbeam_moe.so")
 
 MOE_OK = 0
-MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8 = 0, 1, 2
+MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8, MOE_W_NVFP4_A4 = 0, 1, 2, 3
 MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_EXPERTS, MOE_OP_FORWARD = 0, 1, 2, 3
 MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
 
 EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
             "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
             "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_bias_update",
-            "moe_permute_noalloc")
+            "moe_quantize_nvfp4", "moe_permute_noalloc")
 
 
 class MoeDims(ctypes.Structure):
@@ -41,7 +41,8 @@ class MoeExperts(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int),
                 ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
-                ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p)]
+                ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p),
+                ("x_global", ctypes.c_float), ("h_global", ctypes.c_float)]
 
 
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -58,6 +59,7 @@ _sig = {
     "moe_experts_swiglu": ([_DP, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "moe_combine": ([_DP, _P, _P, _P, _P], _I),
     "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
+    "moe_quantize_nvfp4": ([_I, _I, _P, ctypes.c_float, _P, _P, _P], _I),
     "moe_bias_update": ([_DP, _P, _P, ctypes.c_double, _I, _I, ctypes.POINTER(ctypes.c_float), _P], _I),
     "moe_permute_noalloc": ([_DP, _P, _P, _P, _P, _P, _P, _P], _I),
 }
@@ -166,6 +168,8 @@ class Experts:
     bf16: w_gate, w_up [E, I, H], w_down [E, H, I].
     NVFP4: w_* packed e2m1 uint8 [E, N, K/2], s_* e4m3 uint8 [E, N, K/16], g_* fp32 [E].
     FP8: w_* e4m3 uint8 [E, N, K], s_* None, g_* fp32 [E, N] row scales.
+    a4 = (x_global, h_global) with NVFP4 weights selects W4A4: x and h are
+    quantised to NVFP4 with those static global scales.
     """
     w_gate: torch.Tensor
     w_up: torch.Tensor
@@ -176,12 +180,15 @@ class Experts:
     g_gate: Optional[torch.Tensor] = None
     g_up: Optional[torch.Tensor] = None
     g_down: Optional[torch.Tensor] = None
+    a4: Optional[tuple] = None
 
     @property
     def dtype(self) -> int:
         if self.w_gate.dtype != torch.uint8:
             return MOE_W_BF16
-        return MOE_W_NVFP4 if self.s_gate is not None else MOE_W_FP8
+        if self.s_gate is None:
+            return MOE_W_FP8
+        return MOE_W_NVFP4 if self.a4 is None else MOE_W_NVFP4_A4
 
     def struct(self, d: MoeDims) -> MoeExperts:
         E, H, I = d.E, d.H, d.I
@@ -199,7 +206,8 @@ class Experts:
                               _ptr(self.g_gate, f32, (E, I), "g_gate"),
                               _ptr(self.g_up, f32, (E, I), "g_up"),
                               _ptr(self.g_down, f32, (E, H), "g_down"))
-        return MoeExperts(MOE_W_NVFP4,
+        gx, gh = self.a4 if self.a4 is not None else (0.0, 0.0)
+        return MoeExperts(self.dtype,
                           _ptr(self.w_gate, u8, (E, I, H // 2), "w_gate"),
                           _ptr(self.w_up, u8, (E, I, H // 2), "w_up"),
                           _ptr(self.w_down, u8, (E, H, I // 2), "w_down"),
@@ -207,7 +215,7 @@ class Experts:
                           _ptr(self.s_up, u8, (E, I, H // 16), "s_up"),
                           _ptr(self.s_down, u8, (E, H, I // 16), "s_down"),
                           _ptr(self.g_gate, f32, (E,), "g_gate"), _ptr(self.g_up, f32, (E,), "g_up"),
-                          _ptr(self.g_down, f32, (E,), "g_down"))
+                          _ptr(self.g_down, f32, (E,), "g_down"), float(gx), float(gh))
 
 
 def moe_route(d: MoeDims, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
@@ -276,6 +284,17 @@ def moe_bias_update(d: MoeDims, topk_idx, bias, gamma_max: float, step: int, tot
         _ptr(bias, torch.float32, (d.E,), "bias"), float(gamma_max), int(step), int(total_steps),
         ctypes.byref(g), _stream(stream)))
     return g.value
+
+
+def moe_quantize_nvfp4(x, g: float, q, s, stream=None):
+    """NVFP4 quantisation of bf16 rows x [rows, cols] with global scale g:
+    fills q uint8 [rows, cols/2] (even column in the low nibble) and
+    s uint8 [rows, cols/16] (e4m3 scale codes)."""
+    rows, cols = x.shape
+    _check("moe_quantize_nvfp4", native().moe_quantize_nvfp4(
+        rows, cols, _ptr(x, torch.bfloat16, (rows, cols), "x"), float(g),
+        _ptr(q, torch.uint8, (rows, cols // 2), "q"), _ptr(s, torch.uint8, (rows, cols // 16), "s"),
+        _stream(stream)))
 
 
 def moe_permute_noalloc(d: MoeDims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src,

@@ -33,6 +33,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
+bool finite_positive(float v) { return v > 0.0f && v <= 3.402823466e38f; }
+
 }  // namespace
 
 bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
@@ -118,8 +120,11 @@ moe_status check_experts(const moe_dims *d, const moe_experts *ex) {
     if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down})) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
   }
-  if (ex->dtype == MOE_W_NVFP4) {
+  if (ex->dtype == MOE_W_NVFP4 || ex->dtype == MOE_W_NVFP4_A4) {
     if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down, ex->s_gate, ex->s_up, ex->s_down}))
+      return MOE_ERR_INVALID_ARG;
+    if (ex->dtype == MOE_W_NVFP4_A4 &&
+        !(finite_positive(ex->x_global) && finite_positive(ex->h_global)))
       return MOE_ERR_INVALID_ARG;
     for (const float *g : {ex->g_gate, ex->g_up, ex->g_down})
       if (!g || (reinterpret_cast<uintptr_t>(g) & 3u)) return MOE_ERR_INVALID_ARG;
@@ -159,7 +164,9 @@ moe_status moe_check_dims(const moe_dims *dims) { return check_dims(dims); }
 
 size_t moe_workspace_size(const moe_dims *dims, moe_wdtype wdtype, moe_op op) {
   if (check_dims(dims) != MOE_OK) return 0;
-  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_NVFP4 && wdtype != MOE_W_FP8) return 0;
+  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_NVFP4 && wdtype != MOE_W_FP8 &&
+      wdtype != MOE_W_NVFP4_A4)
+    return 0;
   if (op < MOE_OP_ROUTE || op > MOE_OP_FORWARD) return 0;
   return ws_layout(*dims, op, wdtype).total;
 }
@@ -221,6 +228,15 @@ moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts, 
   if ((st = check_ws(dims, MOE_OP_EXPERTS, ws, ws_bytes, experts->dtype)) != MOE_OK) return st;
   const WsLayout L = ws_layout(*dims, MOE_OP_EXPERTS, experts->dtype);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (experts->dtype == MOE_W_NVFP4_A4) {
+    uint8_t *xq = at<uint8_t>(ws, L.xq), *xs = at<uint8_t>(ws, L.xs);
+    const int Tk = dims->T * dims->top_k;
+    if ((st = launch_quantize_nvfp4(x_perm, nullptr, nullptr, dims->E, dims->top_k, Tk, dims->H,
+                                    experts->x_global, xq, xs, s)) != MOE_OK)
+      return st;
+    return launch_experts_w4a4(*dims, *experts, xq, xs, expert_offsets, row_src, topk_w, y_partial,
+                               at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status_word(ws), s);
+  }
   if (experts->dtype != MOE_W_BF16) {
     void *x16 = at<void>(ws, L.x16);
     const size_t n = (size_t)dims->T * dims->top_k * dims->H;
@@ -254,7 +270,8 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   if ((st = check_ws(dims, MOE_OP_FORWARD, ws, ws_bytes, experts->dtype)) != MOE_OK) return st;
   const moe_dims &d = *dims;
   const WsLayout L = ws_layout(d, MOE_OP_FORWARD, experts->dtype);
-  const bool fp4 = experts->dtype != MOE_W_BF16;  // packed weights: NVFP4 or FP8
+  const bool a4 = experts->dtype == MOE_W_NVFP4_A4;
+  const bool fp4 = experts->dtype != MOE_W_BF16 && !a4;  // packed weights, f16 activations
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t *idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
   float *w = topk_w ? topk_w : at<float>(ws, L.topk_w);
@@ -266,12 +283,21 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   int32_t *offsets = at<int32_t>(ws, L.offsets);
   int32_t *slot_of = at<int32_t>(ws, L.slot_of);
   int32_t *row_src = at<int32_t>(ws, L.row_src);
-  // with NVFP4 weights the gather writes x_perm in f16, the GEMMs' operand type
+  // with NVFP4 or FP8 weights the gather writes x_perm in f16, the GEMMs'
+  // operand type; W4A4 quantises the rows while gathering them
+  const GatherMode gm = a4 ? kGatherNone : fp4 ? kGatherF16 : kGatherBf16;
   if ((st = launch_permute(d, idx, x, x_perm, offsets, slot_of, row_src, at<int32_t>(ws, L.counts),
-                           at<int32_t>(ws, L.bases), status, s, fp4)) != MOE_OK)
+                           at<int32_t>(ws, L.bases), status, s, gm)) != MOE_OK)
     return st;
   void *y_partial = at<void>(ws, L.y_partial);
-  if (fp4)
+  if (a4) {
+    uint8_t *xq = at<uint8_t>(ws, L.xq), *xs = at<uint8_t>(ws, L.xs);
+    if ((st = launch_quantize_nvfp4(x, row_src, offsets, d.E, d.top_k, d.T * d.top_k, d.H,
+                                    experts->x_global, xq, xs, s)) != MOE_OK)
+      return st;
+    st = launch_experts_w4a4(d, *experts, xq, xs, offsets, row_src, w, y_partial,
+                             at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status, s);
+  } else if (fp4)
     st = launch_experts_fp4(d, *experts, x_perm, offsets, row_src, w, y_partial, at<void>(ws, L.h),
                             status, s);
   else
@@ -279,6 +305,15 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
                         at<__nv_bfloat16>(ws, L.h), status, s);
   if (st != MOE_OK) return st;
   return launch_combine(d, y_partial, slot_of, y, s);
+}
+
+moe_status moe_quantize_nvfp4(int rows, int cols, const void *x, float g, uint8_t *q, uint8_t *s,
+                              moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || !finite_positive(g)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!ptrs_ok({x, q, s})) return MOE_ERR_INVALID_ARG;
+  return launch_quantize_nvfp4(x, nullptr, nullptr, 0, 1, rows, cols, g, q, s,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

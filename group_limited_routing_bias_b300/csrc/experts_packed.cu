@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
+#include "sched.cuh"
 #include "tc_gemm.cuh"
 
 namespace beam {
@@ -160,49 +161,6 @@ __device__ __forceinline__ void tmem_ld_n<16>(uint32_t taddr, uint32_t (&r)[16])
   tmem_ld16(taddr, r);
 }
 
-struct Fp4Sched {
-  int off[257];  // expert row offsets
-  int tp[257];   // prefix of tiles (or token tiles) per expert
-};
-
-// Prefix over experts of ceil(rows_e / rows_per_tile) * mult, computed by warp 0.
-__device__ __forceinline__ void fp4_prologue(const int32_t *offsets, int E, int rows_per_tile,
-                                             int mult, Fp4Sched &s) {
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s.off[i] = offsets[i];
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per;
-    int local = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e)
-      local += (s.off[e + 1] - s.off[e] + rows_per_tile - 1) / rows_per_tile * mult;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-      s.tp[e] = run;
-      run += (s.off[e + 1] - s.off[e] + rows_per_tile - 1) / rows_per_tile * mult;
-    }
-    if (lane == 31) s.tp[E] = incl;
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ int fp4_find_expert(const Fp4Sched &s, int E, int v) {
-  int lo = 0, hi = E;  // last e with tp[e] <= v
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s.tp[mid] <= v) lo = mid;
-    else hi = mid;
-  }
-  return lo;
-}
-
 struct Fp4Params {
   CUtensorMap tmap_act;  // f16 token rows [Tk, K] (x or h), 128-byte swizzle
   CUtensorMap tmap_q0;   // packed codes [E*N, K/2] of W_gate or W_down
@@ -239,21 +197,21 @@ struct ExpertGemmFP4 {
   static constexpr int OPERAND_BYTES = StageGeom<BN, NA>::kBytes;
   static constexpr int STAGES = OPERAND_BYTES * 3 <= 110 * 1024 ? 3 : 2;
   static constexpr int RSTAGES_FIT =
-      (kSmemLimit - kSmemReserve - (int)sizeof(Fp4Sched) - STAGES * OPERAND_BYTES) / RAW_BYTES;
+      (kSmemLimit - kSmemReserve - (int)sizeof(TileSched) - STAGES * OPERAND_BYTES) / RAW_BYTES;
   static constexpr int RSTAGES = RSTAGES_FIT > 16 ? 16 : RSTAGES_FIT;
   static_assert(RSTAGES >= 2, "raw ring needs two slots");
 
   using Params = Fp4Params;
-  using Sched = Fp4Sched;
+  using Sched = TileSched;
   struct Tile {
     int row0, nrows, arow0, m, e;
   };
 
-  __device__ static void prologue(const Params &p, Sched &s) { fp4_prologue(p.offsets, p.E, BN, 1, s); }
+  __device__ static void prologue(const Params &p, Sched &s) { tile_sched_prologue(p.offsets, p.E, BN, 1, s); }
   __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E] * p.mt; }
   __device__ static Tile tile(const Params &p, const Sched &s, int t) {
     const int tti = t / p.mt, m = t - tti * p.mt;
-    const int e = fp4_find_expert(s, p.E, tti);
+    const int e = tile_sched_expert(s, p.E, tti);
     const int row0 = s.off[e] + (tti - s.tp[e]) * BN;
     return Tile{row0, min(BN, s.off[e + 1] - row0), e * p.w_rows + m * kTileM, m, e};
   }
@@ -320,24 +278,24 @@ struct ExpertGemmTMFP4 {
   static constexpr int TX_BYTES = kATileBytes;  // the activation tile; raw bytes on their own ring
   static constexpr int NBUF = 2;
   static constexpr int STAGES = 3;
-  static constexpr int RSTAGES_FIT = (kSmemLimit - kSmemReserve - (int)sizeof(Fp4Sched) -
+  static constexpr int RSTAGES_FIT = (kSmemLimit - kSmemReserve - (int)sizeof(TileSched) -
                                       STAGES * StageGeom<BN, NA>::kBytes) / RAW_BYTES;
   static constexpr int RSTAGES = RSTAGES_FIT > 16 ? 16 : RSTAGES_FIT;
   static_assert(RSTAGES >= 2, "raw ring needs two slots");
   static constexpr int FW = GATEUP ? 128 : 256;
 
   using Params = Fp4Params;
-  using Sched = Fp4Sched;
+  using Sched = TileSched;
   struct Tile {
     int row0, nrows, brow0, f, e;
   };
 
   __device__ static void prologue(const Params &p, Sched &s) {
-    fp4_prologue(p.offsets, p.E, kTileM, p.mt, s);
+    tile_sched_prologue(p.offsets, p.E, kTileM, p.mt, s);
   }
   __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E]; }
   __device__ static Tile tile(const Params &p, const Sched &s, int t) {
-    const int e = fp4_find_expert(s, p.E, t);
+    const int e = tile_sched_expert(s, p.E, t);
     const int ntt = (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM;
     const int local = t - s.tp[e];
     const int f = local / ntt, tt = local - f * ntt;

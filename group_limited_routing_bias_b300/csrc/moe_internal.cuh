@@ -60,6 +60,7 @@ struct WsLayout {
   size_t offsets = 0, slot_of = 0, row_src = 0, x_perm = 0;  // forward only
   size_t h = 0;                                     // experts
   size_t x16 = 0;                                   // experts, NVFP4 only
+  size_t xq = 0, xs = 0, hq = 0, hs = 0;            // experts and forward, W4A4 only
   size_t y_partial = 0;                             // forward only
   size_t total = 0;
 };
@@ -88,14 +89,22 @@ inline WsLayout ws_layout(const moe_dims &d, moe_op op, moe_wdtype wdtype = MOE_
     L.counts = take(nchunks * d.E * 4);
     L.bases = take(nchunks * d.E * 4);
   }
+  const bool a4 = wdtype == MOE_W_NVFP4_A4;
   if (fwd) {
     L.offsets = take((size_t)(d.E + 1) * 4);
     L.slot_of = take(Tk * 4);
     L.row_src = take(Tk * 4);
-    L.x_perm = take(Tk * d.H * 2);
+    if (!a4) L.x_perm = take(Tk * d.H * 2);
   }
-  if (op == MOE_OP_EXPERTS || fwd) L.h = take(Tk * d.I * 2);
-  if (op == MOE_OP_EXPERTS && wdtype != MOE_W_BF16) L.x16 = take(Tk * d.H * 2);
+  if (a4 && (op == MOE_OP_EXPERTS || fwd)) {
+    L.xq = take(Tk * d.H / 2);
+    L.xs = take(Tk * d.H / 16);
+    L.hq = take(Tk * d.I / 2);
+    L.hs = take(Tk * d.I / 16);
+  } else if (op == MOE_OP_EXPERTS || fwd) {
+    L.h = take(Tk * d.I * 2);
+  }
+  if (op == MOE_OP_EXPERTS && wdtype != MOE_W_BF16 && !a4) L.x16 = take(Tk * d.H * 2);
   if (fwd) L.y_partial = take(Tk * d.H * 2);
   L.total = off;
   return L;
@@ -122,10 +131,28 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
                         int32_t *topk_idx, float *topk_w, const RouterPlan &rp,
                         __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream);
 
+// What the dispatch does with x after sorting: copy rows in bf16, copy them
+// as f16 (operands of the packed-weight GEMMs), or nothing (W4A4 quantises
+// while gathering, in launch_quantize_nvfp4).
+enum GatherMode { kGatherBf16 = 0, kGatherF16 = 1, kGatherNone = 2 };
+
 moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
                           int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
                           int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream,
-                          bool f16_out = false);
+                          GatherMode gather = kGatherBf16);
+
+// NVFP4 quantisation of bf16 rows.  With row_src, output row r (r < offsets[E],
+// read on the device) is x[row_src[r] / top_k]; otherwise row r is x[r], r < rows.
+moe_status launch_quantize_nvfp4(const void *x, const int32_t *row_src, const int32_t *offsets,
+                                 int E, int top_k, int rows, int cols, float g, uint8_t *q,
+                                 uint8_t *s, cudaStream_t stream);
+
+// NVFP4 weights and activations: xq/xs the quantised permuted rows, hq/hs
+// scratch for the quantised h.
+moe_status launch_experts_w4a4(const moe_dims &d, const moe_experts &ex, const uint8_t *xq,
+                               const uint8_t *xs, const int32_t *offsets, const int32_t *row_src,
+                               const float *topk_w, void *y_partial, uint8_t *hq, uint8_t *hs,
+                               uint32_t *status, cudaStream_t stream);
 
 moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *x_perm,
                           const int32_t *expert_offsets, const int32_t *row_src,

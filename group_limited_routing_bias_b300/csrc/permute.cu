@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(256)
 moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
                           int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
                           int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream,
-                          bool f16_out) {
+                          GatherMode gather) {
   const int Tk = d.T * d.top_k;
   const int nchunks = std::max(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
   static bool attr_set = false;
@@ -253,9 +253,9 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
     permute_scatter_kernel<<<nchunks, kChunkThreads, scatter_smem, stream>>>(
         topk_idx, Tk, d.E, bases, slot_of, row_src);
   }
-  if (Tk > 0) {
+  if (Tk > 0 && gather != kGatherNone) {
     const int blocks = std::max(1, std::min((Tk + 7) / 8, device_sm_count() * 8));
-    if (f16_out)
+    if (gather == kGatherF16)
       permute_gather_kernel<true><<<blocks, 256, 0, stream>>>(
           static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
           static_cast<uint4 *>(x_perm));

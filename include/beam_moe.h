@@ -57,6 +57,10 @@
  *                  consecutive k), g_* fp32 [E] global scales; the weight is
  *                  e2m1 * e4m3 * global.  (N, K) = (I, H) for gate and up,
  *                  (H, I) for down.  Needs H % 256 == 0 and I % 256 == 0.
+ *   NVFP4 W4A4:    the NVFP4 layouts above, plus x_global and h_global in
+ *                  moe_experts; the activations are quantised as in
+ *                  moe_quantize_nvfp4, the GEMMs accumulate in fp32, and h is
+ *                  held as NVFP4 between them.
  *   FP8 experts:   w_* e4m3 uint8 [E, N, K]; g_* fp32 [E, N], one scale per
  *                  output row (the pages give no FP8 layout: this is the plain
  *                  reading that keeps dequantisation exact); s_* unused.
@@ -84,7 +88,10 @@ typedef enum {
   MOE_ERR_NOT_IMPLEMENTED = 6
 } moe_status;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_FP8 = 2 } moe_wdtype;
+/* Expert weight formats.  MOE_W_NVFP4_A4 takes NVFP4 weights as MOE_W_NVFP4
+ * and also quantises the activations (x before gate/up, h before down) to
+ * NVFP4, so both GEMMs run on the block-scaled fp4 tensor cores (W4A4). */
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_FP8 = 2, MOE_W_NVFP4_A4 = 3 } moe_wdtype;
 
 /* Which entry point a workspace is sized for. */
 typedef enum {
@@ -115,6 +122,9 @@ typedef struct {
   const uint8_t *s_gate, *s_up, *s_down; /* e4m3 block scales (NVFP4 only)          */
   const float *g_gate, *g_up, *g_down;   /* fp32 [E] globals (NVFP4), [E, N] row
                                             scales (FP8)                            */
+  float x_global, h_global;              /* MOE_W_NVFP4_A4 only: static fp32 global
+                                            scales of the x and h quantisers (finite,
+                                            > 0; see moe_quantize_nvfp4)            */
 } moe_experts;
 
 /* Library version, major * 10000 + minor * 100 + patch. */
@@ -218,6 +228,25 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
 moe_status moe_bias_update(const moe_dims *dims, const int32_t *topk_idx, float *bias,
                            double gamma_max, int step, int total_steps, float *gamma_used,
                            moe_stream_t stream);
+
+/*
+ * NVFP4 quantisation of activations, the step MOE_W_NVFP4_A4 applies to x
+ * before the gate/up GEMM and to h before the down GEMM.  The pages give only
+ * "NVFP4 for Blackwell" ("Reflection Releases Beam ...", section "Where Beam
+ * Saves and Where the Memory Bill Comes In"); the reading here is the
+ * weights' two-level format with a static per-tensor global scale g:
+ * for every block of 16 consecutive values v of a row, in fp32 (IEEE
+ * division and multiplication, round to nearest even):
+ *   amax = max |v|;  s = e4m3(amax / (6 g)) saturating at 448;
+ *   scale = value(s) * g;  code_i = e2m1(v_i / scale) saturating at +-6
+ *   (all codes 0 when scale == 0).  The value of a code is e2m1 * e4m3 * g.
+ *   x  bf16 [rows, cols] (cols % 16 == 0), g finite and > 0
+ *   q  uint8 [rows, cols/2]: two codes per byte, even column in the low nibble
+ *   s  uint8 [rows, cols/16]: e4m3 scale codes
+ * Needs no workspace.  rows == 0 is a no-op.
+ */
+moe_status moe_quantize_nvfp4(int rows, int cols, const void *x, float g, uint8_t *q, uint8_t *s,
+                              moe_stream_t stream);
 
 /*
  * moe_permute_noalloc — the dispatch of moe_permute for callers that cannot

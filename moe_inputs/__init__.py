@@ -71,6 +71,14 @@ CONFIGS = {
 }
 NVFP4_TOKENS = (1, 64, 1024, 16384)
 
+# Static global scales of the W4A4 activation quantisers (the calibrated
+# input scales an NVFP4 checkpoint carries): the largest magnitude each tensor's
+# block scales must reach, over e4m3_max * e2m1_max = 448 * 6.  With these
+# inputs x ~ N(0, 1) stays below 8 in magnitude, and h = silu(g) * u with
+# g, u ~ N(0, 1) (weights ~ N(0, 1/fan_in)) below 32.
+A4_X_GLOBAL = 8.0 / 2688.0
+A4_H_GLOBAL = 32.0 / 2688.0
+
 
 def _gen(seed: int, device="cpu") -> torch.Generator:
     g = torch.Generator(device=device)
