@@ -15,7 +15,7 @@
 // and quantises it to NVFP4 (16 consecutive features per scale) for the down
 // GEMM.  Down scales each token row by its routing weight and stores bf16.
 //
-// One CTA per SM, persistent; 384 threads:
+// One CTA per SM, persistent; 640 threads:
 //   warp 0 lane 0 : TMA producer (codes with the 128-byte swizzle, scales plain)
 //   warp 1        : MMA warp.  All lanes rearrange each stage's scale bytes in
 //                   shared memory into the 32 x 16-byte blocks that
@@ -24,7 +24,7 @@
 //                   its four 16-k scales in consecutive bytes); lane 0 issues
 //                   the copies and the four K=64 MMAs of the stage.
 //   warp 2        : tensor-memory allocation
-//   warps 4..11   : epilogue, two warps per 32-lane quarter of the accumulator
+//   warps 4..19   : epilogue, four warps per 32-lane quarter of the accumulator
 // Tensor memory: accumulator columns [0, 256); stage s keeps its scales at
 // columns 256 + 48 s: A in the first 16 (4 per MMA), B in the next 32 (8 per
 // MMA, one column per 32 rows of N).  A stage's scale columns are rewritten
@@ -49,7 +49,7 @@ constexpr int kW4SfABytes = kW4M * 16;             // 2 KB: 16 scales per row pe
 constexpr int kW4SfBBytes = kW4N * 16;             // 4 KB
 constexpr int kW4Stage = kW4ABytes + kW4BBytes + kW4SfABytes + kW4SfBBytes;  // 55296
 constexpr int kW4Stages = 4;
-constexpr int kW4EpiWarps = 8;
+constexpr int kW4EpiWarps = 16;
 constexpr int kW4Threads = 128 + 32 * kW4EpiWarps;
 constexpr uint32_t kW4TmemCols = 512;
 constexpr uint32_t kW4SfCol0 = 256;
@@ -293,9 +293,12 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
       mbar_drain_wait(drain, 0);
     }
   } else if (warp >= 4) {
-    // ---------------- epilogue
+    // ---------------- epilogue: four warps per 32-lane quarter, each with a
+    // quarter of the tile's output columns.  A warp copies its accumulator
+    // columns into registers and releases tensor memory at once, so the next
+    // tile's MMAs overlap the SwiGLU / quantisation / stores below.
     const int q = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int part = (warp - 4) >> 2;  // 0..3
     const int row = q * 32 + lane;
     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
     uint32_t bph = 0;
@@ -303,66 +306,69 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
       const W4Tile tile = w4_tile<GATEUP>(p, *sched, t);
       bool ok = mbar_wait(tfull, bph, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
+      bph ^= 1u;
+      const bool live = q * 32 < tile.nrows;  // this quarter holds rows of the tile
+      uint32_t a[64];
+      if (live) {
+        tc_fence_after();
+        if (GATEUP) {  // gate columns [32 part, +32), up columns 128 + the same
+          tmem_ld32(tq + part * 32, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+          tmem_ld32(tq + 128 + part * 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+        } else {  // output columns [64 part, +64)
+          tmem_ld32(tq + part * 64, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+          tmem_ld32(tq + part * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
+        }
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      if (!live) continue;
       const bool valid = row < tile.nrows;
       const size_t grow = (size_t)(tile.row0 + row);
       if (GATEUP) {
         const float sg = p.ga * __ldg(p.gw0 + tile.e);
         const float su = p.ga * __ldg(p.gw1 + tile.e);
         const float six_gh = 6.0f * p.gh;
-        uint32_t cw[8];
+        uint32_t cw[4];
         uint32_t scw = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int col = half * 64 + c * 16;
-          uint32_t g[16], u[16];
-          tmem_ld16(tq + col, g);
-          tmem_ld16(tq + 128 + col, u);
-          tmem_wait_ld();
-          float h[16];
+        for (int c = 0; c < 2; ++c) {
+          float *h = reinterpret_cast<float *>(&a[c * 16]);  // h overwrites g
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float gv = __uint_as_float(g[i]) * sg;
-            h[i] = gv / (1.0f + __expf(-gv)) * (__uint_as_float(u[i]) * su);
+            const float gv = __uint_as_float(a[c * 16 + i]) * sg;
+            const float uv = __uint_as_float(a[32 + c * 16 + i]) * su;
+            h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
           }
           uint2 codes;
-          const uint32_t sc = nvfp4_quantize_block(h, six_gh, p.gh, codes);
+          const uint32_t sc =
+              nvfp4_quantize_block(*reinterpret_cast<float(*)[16]>(h), six_gh, p.gh, codes);
           cw[2 * c] = codes.x;
           cw[2 * c + 1] = codes.y;
           scw |= sc << (8 * c);
         }
         if (valid) {
-          const int feat0 = tile.f * 128 + half * 64;
-          uint4 *dq = reinterpret_cast<uint4 *>(p.hq + grow * (p.out_cols / 2) + feat0 / 2);
-          dq[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          dq[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-          *reinterpret_cast<uint32_t *>(p.hs + grow * (p.out_cols / 16) + feat0 / 16) = scw;
+          const int feat0 = tile.f * 128 + part * 32;
+          *reinterpret_cast<uint4 *>(p.hq + grow * (p.out_cols / 2) + feat0 / 2) =
+              make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint16_t *>(p.hs + grow * (p.out_cols / 16) + feat0 / 16) =
+              (uint16_t)scw;
         }
-      } else {
-        const float w = valid ? __ldg(p.topk_w + __ldg(p.row_src + tile.row0 + row)) : 0.f;
+      } else if (valid) {
+        const float w = __ldg(p.topk_w + __ldg(p.row_src + tile.row0 + row));
         const float sc = p.ga * __ldg(p.gw0 + tile.e) * w;
-        __nv_bfloat16 *dst = p.y + grow * p.out_cols + tile.f * 256 + half * 128;
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t a[32];
-          tmem_ld32(tq + half * 128 + c, a);
-          tmem_wait_ld();
-          if (valid) {
-            uint32_t pk[16];
+        uint4 *d4 = reinterpret_cast<uint4 *>(p.y + grow * p.out_cols + tile.f * 256 + part * 64);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = pack_bf16x2_w4(__uint_as_float(a[2 * j]) * sc, __uint_as_float(a[2 * j + 1]) * sc);
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+        for (int v = 0; v < 8; ++v) {
+          uint32_t pk[4];
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          for (int j = 0; j < 4; ++j)
+            pk[j] = pack_bf16x2_w4(__uint_as_float(a[8 * v + 2 * j]) * sc,
+                                   __uint_as_float(a[8 * v + 2 * j + 1]) * sc);
+          d4[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-      bph ^= 1u;
     }
   }
 
