@@ -17,13 +17,14 @@
 //
 // One CTA per SM, persistent; 640 threads:
 //   warp 0 lane 0 : TMA producer (codes with the 128-byte swizzle, scales plain)
-//   warp 1        : MMA warp.  All lanes rearrange each stage's scale bytes in
-//                   shared memory into the 32 x 16-byte blocks that
-//                   tcgen05.cp.32x128b.warpx4 copies to tensor memory (row m of
-//                   a 128-row block goes to byte (m % 32) * 16 + (m / 32) * 4,
-//                   its four 16-k scales in consecutive bytes); lane 0 issues
-//                   the copies and the four K=64 MMAs of the stage.
-//   warp 2        : tensor-memory allocation
+//   warp 1 lane 0 : MMA issuer: copies each stage's scales to tensor memory
+//                   (tcgen05.cp) and issues the four K=64 MMAs of the stage
+//   warps 2, 3    : scale arrangers, alternate K slices: rearrange the stage's
+//                   scale bytes in shared memory into the 32 x 16-byte blocks
+//                   that tcgen05.cp.32x128b.warpx4 copies to tensor memory (row
+//                   m of a 128-row block goes to byte (m % 32) * 16 + (m / 32) * 4,
+//                   its four 16-k scales in consecutive bytes); warp 2 also
+//                   allocates tensor memory
 //   warps 4..19   : epilogue, four warps per 32-lane quarter of the accumulator
 // Tensor memory: accumulator columns [0, 256); stage s keeps its scales at
 // columns 256 + 48 s: A in the first 16 (4 per MMA), B in the next 32 (8 per
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
   uint8_t *stages = smem_raw + pad;
   uint64_t *full = reinterpret_cast<uint64_t *>(stages + kW4Stages * kW4Stage);
   uint64_t *empty = full + kW4Stages;
-  uint64_t *tfull = empty + kW4Stages;
+  uint64_t *sfready = empty + kW4Stages;  // a stage's scale factors are arranged
+  uint64_t *tfull = sfready + kW4Stages;
   uint64_t *tempty = tfull + 1;
   uint64_t *drain = tempty + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
     for (int s = 0; s < kW4Stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sfready[s], 1);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, kW4EpiWarps);
@@ -234,33 +237,28 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA warp
-    constexpr uint32_t kIdesc = w4_idesc(kW4M, kW4N);
-    int stage = 0;
-    uint32_t ph = 0, bph = 0;
-    bool ok = true, any = false;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-      bool got = lane != 0 || mbar_wait(tempty, bph ^ 1u, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      for (int k = 0; k < p.ksteps; ++k) {
-        got = mbar_wait(&full[stage], ph, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, got)) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: scale copies to tensor memory, then the MMAs
+      constexpr uint32_t kIdesc = w4_idesc(kW4M, kW4N);
+      int stage = 0;
+      uint32_t ph = 0, bph = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+        if (!mbar_wait(tempty, bph ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        uint8_t *st = stages + stage * kW4Stage;
-        uint8_t *sfa = st + kW4ABytes + kW4BBytes;
-        uint8_t *sfb = sfa + kW4SfABytes;
-        w4_arrange_sf<1>(sfa, lane);
-        w4_arrange_sf<2>(sfb, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        tc_fence_after();
+        for (int k = 0; k < p.ksteps; ++k) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, p.status) ||
+              !mbar_wait(&sfready[stage], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
+          uint8_t *st = stages + stage * kW4Stage;
+          const uint8_t *sfa = st + kW4ABytes + kW4BBytes;
+          const uint8_t *sfb = sfa + kW4SfABytes;
           const uint32_t sf_t = tmem_base + kW4SfCol0 + stage * kW4SfStride;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -275,22 +273,48 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
             umma_fp4(tmem_base, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_t + 4 * j,
                      sf_t + 16 + 8 * j, (k | j) != 0 ? 1u : 0u);
           umma_commit(&empty[stage]);
+          any = true;
+          if (++stage == kW4Stages) {
+            stage = 0;
+            ph ^= 1u;
+          }
         }
-        __syncwarp();
-        any = true;
+        if (!ok) break;
+        umma_commit(tfull);
+        bph ^= 1u;
+      }
+      if (!ok && any) {  // wait for the tensor cores before the memory is released
+        umma_commit(drain);
+        mbar_drain_wait(drain, 0);
+      }
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- scale arrangers: warp 2 takes the even K slices of the
+    // CTA's sequence, warp 3 the odd ones, so arranging one slice overlaps the
+    // MMA issue of the previous one.
+    int stage = 0, n = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      for (int k = 0; k < p.ksteps; ++k, ++n) {
+        if ((n & 1) == warp - 2) {
+          const bool got = mbar_wait(&full[stage], ph, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sfa = stages + stage * kW4Stage + kW4ABytes + kW4BBytes;
+          w4_arrange_sf<1>(sfa, lane);
+          w4_arrange_sf<2>(sfa + kW4SfABytes, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfready[stage]);
+        }
         if (++stage == kW4Stages) {
           stage = 0;
           ph ^= 1u;
         }
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(tfull);
-      __syncwarp();
-      bph ^= 1u;
-    }
-    if (!ok && any && lane == 0) {  // wait for the tensor cores before the memory is released
-      umma_commit(drain);
-      mbar_drain_wait(drain, 0);
     }
   } else if (warp >= 4) {
     // ---------------- epilogue: four warps per 32-lane quarter, each with a
