@@ -284,7 +284,7 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   int32_t *slot_of = at<int32_t>(ws, L.slot_of);
   int32_t *row_src = at<int32_t>(ws, L.row_src);
   // with NVFP4 or FP8 weights the gather writes x_perm in f16, the GEMMs'
-  // operand type; W4A4 quantises the rows while gathering them
+  // operand type; W4A4 quantises each token once and writes it to its slots
   const GatherMode gm = a4 ? kGatherNone : fp4 ? kGatherF16 : kGatherBf16;
   if ((st = launch_permute(d, idx, x, x_perm, offsets, slot_of, row_src, at<int32_t>(ws, L.counts),
                            at<int32_t>(ws, L.bases), status, s, gm)) != MOE_OK)
@@ -292,8 +292,8 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   void *y_partial = at<void>(ws, L.y_partial);
   if (a4) {
     uint8_t *xq = at<uint8_t>(ws, L.xq), *xs = at<uint8_t>(ws, L.xs);
-    if ((st = launch_quantize_nvfp4(x, row_src, offsets, d.E, d.top_k, d.T * d.top_k, d.H,
-                                    experts->x_global, xq, xs, s)) != MOE_OK)
+    if ((st = launch_quantize_scatter_nvfp4(x, slot_of, d.T, d.top_k, d.H, experts->x_global, xq,
+                                            xs, s)) != MOE_OK)
       return st;
     st = launch_experts_w4a4(d, *experts, xq, xs, offsets, row_src, w, y_partial,
                              at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status, s);

@@ -438,7 +438,59 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The dispatch's form for the forward pass: token t is quantised once and its
+// codes and scales are written to every permuted row that holds one of its
+// entries (slot_of[t*k + j]; dropped entries have slot -1).  One warp per token.
+__global__ void __launch_bounds__(256)
+    quantize_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
+                            int T, int top_k, int cols, float g, uint2 *__restrict__ q,
+                            uint8_t *__restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int nblk = cols / 16;
+  const float six_g = 6.0f * g;
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    const uint4 *xr = x + (size_t)t * (cols / 8);
+    const int my_slot = lane < top_k ? __ldg(slot_of + (size_t)t * top_k + lane) : -1;
+    for (int b0 = 0; b0 < nblk; b0 += 32) {  // whole warp each step: the slots are shuffled
+      const int b = b0 + lane;
+      uint2 codes = make_uint2(0u, 0u);
+      uint8_t sc = 0;
+      if (b < nblk) {
+        const uint4 lo = xr[2 * b], hi = xr[2 * b + 1];
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+        sc = (uint8_t)nvfp4_quantize_block(v, six_g, g, codes);
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+        if (slot >= 0 && b < nblk) {
+          q[(size_t)slot * nblk + b] = codes;
+          s[(size_t)slot * nblk + b] = sc;
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+moe_status launch_quantize_scatter_nvfp4(const void *x, const int32_t *slot_of, int T, int top_k,
+                                         int cols, float g, uint8_t *q, uint8_t *s,
+                                         cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  const int blocks = std::max(1, std::min((T + 7) / 8, device_sm_count() * 8));
+  quantize_scatter_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(x), slot_of, T,
+                                                     top_k, cols, g, reinterpret_cast<uint2 *>(q),
+                                                     s);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 moe_status launch_quantize_nvfp4(const void *x, const int32_t *row_src, const int32_t *offsets,
                                  int E, int top_k, int rows, int cols, float g, uint8_t *q,

@@ -147,6 +147,12 @@ moe_status launch_quantize_nvfp4(const void *x, const int32_t *row_src, const in
                                  int E, int top_k, int rows, int cols, float g, uint8_t *q,
                                  uint8_t *s, cudaStream_t stream);
 
+// NVFP4 quantisation of bf16 token rows x [T, cols], each written to the
+// permuted rows slot_of[t*top_k + j] (skipping -1): the forward's gather.
+moe_status launch_quantize_scatter_nvfp4(const void *x, const int32_t *slot_of, int T, int top_k,
+                                         int cols, float g, uint8_t *q, uint8_t *s,
+                                         cudaStream_t stream);
+
 // NVFP4 weights and activations: xq/xs the quantised permuted rows, hq/hs
 // scratch for the quantised h.
 moe_status launch_experts_w4a4(const moe_dims &d, const moe_experts &ex, const uint8_t *xq,
