@@ -24,6 +24,9 @@
 // A problem class P supplies the shapes and the tile schedule:
 //   static constexpr int BN, NA, STAGES, NBUF, TX_BYTES;
 //   static constexpr bool CONVERT, F16;   (packed weights; f16 instead of bf16 operands)
+//   static constexpr int KSUB;            (optional, default 1: 64-wide K slices per stage;
+//                                          two let each weight row arrive as 256 contiguous
+//                                          bytes per stage, which HBM streams better)
 //   static constexpr int RSTAGES, RAW_BYTES;  (CONVERT: raw ring depth and slot size)
 //   struct Params { ...; uint32_t *status; };  struct Sched;  struct Tile;
 //   static void prologue(const Params&, Sched&)   (all threads; may __syncthreads)
@@ -38,6 +41,8 @@
 //   static void convert(const Params&, const Tile&, int k, uint8_t *stage, const uint8_t *raw,
 //                       int ctid)   (ctid 0..255)
 #pragma once
+
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -56,9 +61,19 @@ struct StageGeom {
   static_assert(kBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 };
 
+template <class P, class = void>
+struct KSubOf {
+  static constexpr int value = 1;
+};
+template <class P>
+struct KSubOf<P, std::void_t<decltype(P::KSUB)>> {
+  static constexpr int value = P::KSUB;
+};
+
+// A stage holds KSUB consecutive 64-wide K slices, each laid out as StageGeom.
 template <class P>
 __host__ __device__ constexpr int stage_bytes_of() {
-  return StageGeom<P::BN, P::NA>::kBytes;
+  return StageGeom<P::BN, P::NA>::kBytes * KSubOf<P>::value;
 }
 
 template <class P>
@@ -91,6 +106,7 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   constexpr uint32_t kTmemCols = tmem_cols_pow2(P::NBUF * kAccCols);
   constexpr uint32_t kIdesc = P::F16 ? umma_idesc_f16(kTileM, P::BN) : umma_idesc_bf16(kTileM, P::BN);
   static_assert(P::NBUF * kAccCols <= 512, "accumulators exceed tensor memory");
+  static_assert(KSubOf<P>::value == 1 || !P::CONVERT, "several K slices per stage: bf16 path only");
   static_assert(P::BN % 16 == 0 && P::BN >= 16 && P::BN <= 256, "invalid MMA N");
 
   extern __shared__ uint8_t smem_raw[];
@@ -217,15 +233,19 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(stages + stage * STAGE);
-          const uint64_t bdesc = umma_desc_sw128(sa + P::NA * kATileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
+          for (int sub = 0; sub < KSubOf<P>::value; ++sub) {
+            const uint32_t sa =
+                smem_u32(stages + stage * STAGE) + sub * StageGeom<P::BN, P::NA>::kBytes;
+            const uint64_t bdesc = umma_desc_sw128(sa + P::NA * kATileBytes);
 #pragma unroll
-            for (int a = 0; a < P::NA; ++a) {
-              const uint64_t adesc = umma_desc_sw128(sa + a * kATileBytes);
-              umma_bf16(d0 + a * P::BN, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
-                        (k | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+#pragma unroll
+              for (int a = 0; a < P::NA; ++a) {
+                const uint64_t adesc = umma_desc_sw128(sa + a * kATileBytes);
+                umma_bf16(d0 + a * P::BN, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                          (k | kk | sub) != 0 ? 1u : 0u);
+              }
             }
           }
           umma_commit(&empty[stage]);
