@@ -6,9 +6,12 @@ and group-limited top-k, dispatch, SwiGLU experts, combine) on B300 GPUs.
 
 A step is one full moe_forward over one batch of the decode workload
 (T=64 tokens at the Beam shape: H=5120, 256 experts in 8 groups of 32, top 4
-groups, top 8 experts, intermediate 2560, bf16 weights, 20 GB per layer).
-Inputs are resident in HBM when the timed region starts; L2 is flushed (a
-512 MB write) before every timed step, outside the step's events.  With
+groups, top 8 experts, intermediate 2560, bf16 weights, 20 GB per layer),
+replayed from a CUDA graph of that one call (the C ABI allocates nothing and
+never synchronises, so it captures; a serving loop would replay it the same
+way); the eager call's time is reported beside it.  Inputs are resident in HBM
+when the timed region starts; L2 is flushed (a 512 MB write) before every
+timed step, outside the step's events.  With
 N > 1 (torchrun) every rank runs an independent replica on its own GPU
 (the path has no exchange step); the value counts all ranks' tokens over
 the slowest rank's time.
@@ -148,6 +151,21 @@ class Workload:
     def forward(self, lib):
         lib.moe_forward(self.d, self.x, self.wr, self.b, self.experts, self.y, self.ws, self.idx,
                         self.w)
+
+
+def capture_forward(lib, wl):
+    """A CUDA graph of one moe_forward of the workload (same buffers)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        wl.forward(lib)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        wl.forward(lib)
+    torch.cuda.synchronize()
+    return g
 
 
 def time_steps(fn, steps, flush):
@@ -482,17 +500,22 @@ def main():
         wl.forward(lib)
     torch.cuda.synchronize()
     assert lib.workspace_status(wl.ws) == 0, "device status set during warm-up"
+    graph = capture_forward(lib, wl)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
     barrier()
     torch.cuda.synchronize()
-    per_step = time_steps(lambda: wl.forward(lib), args.steps, flush)
+    per_step = time_steps(graph.replay, args.steps, flush)
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
     ms, value = aggregate_replicas(statistics.mean(per_step), cfg.T, world, dist, dev)
     assert lib.workspace_status(wl.ws) == 0, "device status set during the timed steps"
+    eager_ms = statistics.mean(time_steps(lambda: wl.forward(lib), args.steps, flush))
 
     if rank != 0:
         if dist is not None:
@@ -557,7 +580,9 @@ def main():
         "config": {"workload": "decode: T=64 tokens, Beam MoE layer (H=5120, E=256 in 8 groups of "
                                "32, top-4 groups, top-8 experts, I=2560, routed scale 2.5), bf16",
                    "T": cfg.T, "l2": "flushed (512 MB write) before every timed step",
+                   "launch": "CUDA graph of one moe_forward call, replayed per step",
                    "parallelism": f"replicas x{world}"},
+        "ms_per_step_eager": eager_ms,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches_per_forward(cfg.T, cfg.top_k) * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4, "fp8": fp8,
     }
