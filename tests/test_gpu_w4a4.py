@@ -177,3 +177,78 @@ def test_w4a4_rejects_bad_globals(lib):
         with pytest.raises(lib.MoeError) as e:
             lib.moe_forward(d, case.x, case.wr, case.b, case.experts(lib, a4), y, ws)
         assert e.value.status == 1
+
+
+def test_w4a4_tiny_skewed(lib):
+    """Strongly skewed load on the W4A4 path: experts with one tile, experts with
+    many, every output compared."""
+    case = A4Case(TINY4, T=1800)
+    case.b_h = mi.zipf_bias(TINY4.E, 0.15, seed=3)
+    case.b = case.b_h.to(DEV)
+    check(lib, case)
+    _, idx, _ = forward(lib, case)
+    load = np.bincount(idx.ravel(), minlength=TINY4.E)
+    assert load.max() > 3 * load.mean()
+
+
+def test_w4a4_beam_skewed_sampled(lib):
+    """The skewed Beam workload (max load ~8x mean) packed to NVFP4, W4A4."""
+    base = mi.CONFIGS["skewed"]
+    cfg = mi.MoeConfig("skewed-w4a4", T=base.T, H=base.H, E=base.E, n_group=base.n_group,
+                       topk_group=base.topk_group, top_k=base.top_k, I=base.I,
+                       routed_scale=base.routed_scale, bias=base.bias, weights="nvfp4",
+                       zipf_alpha=base.zipf_alpha)
+    case = A4Case(cfg)
+    sample = np.sort(np.random.default_rng(7).choice(cfg.T, 48, replace=False))
+    check(lib, case, sample)
+    _, idx, _ = forward(lib, case)
+    load = np.bincount(idx.ravel(), minlength=cfg.E)
+    assert load.max() >= 6 * load.mean()
+
+
+def test_w4a4_other_dims(lib):
+    """A non-Beam shape: 64 experts in 8 groups of 8, keep 3, top 6, H=512, I=768."""
+    cfg = mi.MoeConfig("w4a4-dims", T=300, H=512, E=64, n_group=8, topk_group=3, top_k=6, I=768,
+                       weights="nvfp4")
+    check(lib, A4Case(cfg))
+
+
+def test_w4a4_staged_drops_bad_indices(lib):
+    """Out-of-range expert indices are dropped by the dispatch (status bit set);
+    the W4A4 experts then run on the remaining rows only."""
+    c = TINY4.with_T(96)
+    case = A4Case(c)
+    d = lib.dims_of(c)
+    Tk = c.T * c.top_k
+    idx = torch.empty(c.T, c.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(c.T, c.top_k, dtype=torch.float32, device=DEV)
+    lib.moe_route(d, case.x, case.wr, case.b, idx, w, lib.alloc_workspace(d, lib.MOE_OP_ROUTE))
+    bad = idx.clone()
+    bad[5, 1] = c.E + 3
+    bad[40, 0] = -1
+    x_perm = torch.zeros(Tk, c.H, dtype=torch.bfloat16, device=DEV)
+    offs = torch.empty(c.E + 1, dtype=torch.int32, device=DEV)
+    slot_of = torch.empty(Tk, dtype=torch.int32, device=DEV)
+    row_src = torch.empty(Tk, dtype=torch.int32, device=DEV)
+    ws_p = lib.alloc_workspace(d, lib.MOE_OP_PERMUTE)
+    lib.moe_permute(d, bad, case.x, x_perm, offs, slot_of, row_src, ws_p)
+    assert lib.workspace_status(ws_p) == lib.MOE_DEV_BAD_INDEX
+    assert int(offs[-1]) == Tk - 2
+    y_partial = torch.zeros(Tk, c.H, dtype=torch.bfloat16, device=DEV)
+    ws = lib.alloc_workspace(d, lib.MOE_OP_EXPERTS, lib.MOE_W_NVFP4_A4)
+    lib.moe_experts_swiglu(d, case.experts(lib), x_perm, offs, row_src, w, y_partial, ws)
+    assert lib.workspace_status(ws) == 0
+    # every kept row equals the oracle's W4A4 expert output times its weight
+    rs = row_src.cpu().numpy()[: Tk - 2]
+    ent_t, ent_k = rs // c.top_k, rs % c.top_k
+    bad_np = bad.cpu().numpy()
+    w_np = w.cpu().numpy()
+    xb = mi.bf16_bits(case.x_h)
+    o = np.zeros((Tk - 2, c.H))
+    for e in np.unique(bad_np[ent_t, ent_k]):
+        rows = np.nonzero(bad_np[ent_t, ent_k] == e)[0]
+        o[rows] = oracle.expert_swiglu_w4a4(xb[ent_t[rows]], *case.get_expert(int(e)), *A4)
+    ref = o * w_np[ent_t, ent_k][:, None]
+    got = y_partial.double().cpu().numpy()[: Tk - 2]
+    err = output_errors(got, ref)
+    assert err.ok(), err
