@@ -8,7 +8,7 @@
 //   permute_count_kernel   one CTA per chunk of 4096 entries: histogram
 //   permute_scan_kernel    one CTA: per-chunk bases and expert offsets
 //   permute_scatter_kernel one CTA per chunk: warp-ordered ranks -> slots
-//   permute_gather_kernel  all SMs: copy x rows into x_perm (16-byte vectors)
+//   permute_scatter_rows_kernel  all SMs: each token's x row to its k slots (16-byte vectors)
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
@@ -196,32 +196,41 @@ __global__ void __launch_bounds__(kChunkThreads)
   }
 }
 
-// Copies x rows into permuted order; with TO_F16 the bf16 values are written
-// as f16 (exact for |v| >= 2^-14; the NVFP4 expert GEMMs run on f16 operands).
+// Copies x rows into permuted order, in token order: token t's row is read
+// once and written to every permuted row that holds one of its entries
+// (slot_of[t*k + j]; dropped entries have slot -1).  Reading x once matters
+// when x is larger than L2 (prefill: an expert-ordered gather would fetch each
+// row from DRAM up to k times).  With TO_F16 the bf16 values are written as
+// f16 (exact for |v| >= 2^-14; the packed-weight GEMMs run on f16 operands).
+// One warp per token, one 16-byte vector per lane and step.
 template <bool TO_F16>
 __global__ void __launch_bounds__(256)
-    permute_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ row_src,
-                          const int32_t *__restrict__ offsets, int E, int top_k, int vec_per_row,
-                          uint4 *__restrict__ x_perm) {
-  const int rows = offsets[E];
+    permute_scatter_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
+                                int T, int top_k, int vec_per_row, uint4 *__restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
-    const int t = row_src[r] / top_k;
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    const int my_slot = lane < top_k ? __ldg(slot_of + (size_t)t * top_k + lane) : -1;
     const uint4 *src = x + (size_t)t * vec_per_row;
-    uint4 *dst = x_perm + (size_t)r * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) {
-      uint4 q = src[v];
-      if (TO_F16) {
-        uint32_t *w = reinterpret_cast<uint32_t *>(&q);
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32) {  // whole warp each step: slots are shuffled
+      const int v = v0 + lane;
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      if (v < vec_per_row) {
+        q = src[v];
+        if (TO_F16) {
+          uint32_t *w = reinterpret_cast<uint32_t *>(&q);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-          const __half2 h = __float22half2_rn(f);
-          w[i] = *reinterpret_cast<const uint32_t *>(&h);
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+            const __half2 h = __float22half2_rn(f);
+            w[i] = *reinterpret_cast<const uint32_t *>(&h);
+          }
         }
       }
-      dst[v] = q;
+      for (int j = 0; j < top_k; ++j) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+        if (slot >= 0 && v < vec_per_row) x_perm[(size_t)slot * vec_per_row + v] = q;
+      }
     }
   }
 }
@@ -254,14 +263,14 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
         topk_idx, Tk, d.E, bases, slot_of, row_src);
   }
   if (Tk > 0 && gather != kGatherNone) {
-    const int blocks = std::max(1, std::min((Tk + 7) / 8, device_sm_count() * 8));
+    const int blocks = std::max(1, std::min((d.T + 7) / 8, device_sm_count() * 8));
     if (gather == kGatherF16)
-      permute_gather_kernel<true><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
+      permute_scatter_rows_kernel<true><<<blocks, 256, 0, stream>>>(
+          static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8,
           static_cast<uint4 *>(x_perm));
     else
-      permute_gather_kernel<false><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint4 *>(x), row_src, expert_offsets, d.E, d.top_k, d.H / 8,
+      permute_scatter_rows_kernel<false><<<blocks, 256, 0, stream>>>(
+          static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8,
           static_cast<uint4 *>(x_perm));
   }
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
