@@ -24,11 +24,12 @@ MOE_OK = 0
 MOE_W_BF16, MOE_W_NVFP4, MOE_W_FP8, MOE_W_NVFP4_A4 = 0, 1, 2, 3
 MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_EXPERTS, MOE_OP_FORWARD = 0, 1, 2, 3
 MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
+MOE_LAYOUT_ROWMAJOR, MOE_LAYOUT_TILED = 0, 1
 
 EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
             "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
             "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_bias_update",
-            "moe_quantize_nvfp4", "moe_permute_noalloc")
+            "moe_quantize_nvfp4", "moe_pack_bf16", "moe_permute_noalloc")
 
 
 class MoeDims(ctypes.Structure):
@@ -42,7 +43,8 @@ class MoeExperts(ctypes.Structure):
                 ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
                 ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p),
-                ("x_global", ctypes.c_float), ("h_global", ctypes.c_float)]
+                ("x_global", ctypes.c_float), ("h_global", ctypes.c_float),
+                ("layout", ctypes.c_int)]
 
 
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -60,6 +62,7 @@ _sig = {
     "moe_combine": ([_DP, _P, _P, _P, _P], _I),
     "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
     "moe_quantize_nvfp4": ([_I, _I, _P, ctypes.c_float, _P, _P, _P], _I),
+    "moe_pack_bf16": ([_I, _I, _I, _P, _P, _P], _I),
     "moe_bias_update": ([_DP, _P, _P, ctypes.c_double, _I, _I, ctypes.POINTER(ctypes.c_float), _P], _I),
     "moe_permute_noalloc": ([_DP, _P, _P, _P, _P, _P, _P, _P], _I),
 }
@@ -170,6 +173,7 @@ class Experts:
     FP8: w_* e4m3 uint8 [E, N, K], s_* None, g_* fp32 [E, N] row scales.
     a4 = (x_global, h_global) with NVFP4 weights selects W4A4: x and h are
     quantised to NVFP4 with those static global scales.
+    tiled = True: bf16 weights packed by moe_pack_bf16 (the MMA-tiled layout).
     """
     w_gate: torch.Tensor
     w_up: torch.Tensor
@@ -181,6 +185,7 @@ class Experts:
     g_up: Optional[torch.Tensor] = None
     g_down: Optional[torch.Tensor] = None
     a4: Optional[tuple] = None
+    tiled: bool = False
 
     @property
     def dtype(self) -> int:
@@ -197,7 +202,8 @@ class Experts:
             return MoeExperts(MOE_W_BF16, _ptr(self.w_gate, bf, (E, I, H), "w_gate"),
                               _ptr(self.w_up, bf, (E, I, H), "w_up"),
                               _ptr(self.w_down, bf, (E, H, I), "w_down"), None, None, None, None,
-                              None, None)
+                              None, None, 0.0, 0.0,
+                              MOE_LAYOUT_TILED if self.tiled else MOE_LAYOUT_ROWMAJOR)
         u8, f32 = torch.uint8, torch.float32
         if self.dtype == MOE_W_FP8:
             return MoeExperts(MOE_W_FP8, _ptr(self.w_gate, u8, (E, I, H), "w_gate"),
@@ -295,6 +301,17 @@ def moe_quantize_nvfp4(x, g: float, q, s, stream=None):
         rows, cols, _ptr(x, torch.bfloat16, (rows, cols), "x"), float(g),
         _ptr(q, torch.uint8, (rows, cols // 2), "q"), _ptr(s, torch.uint8, (rows, cols // 16), "s"),
         _stream(stream)))
+
+
+def moe_pack_bf16(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """bf16 expert weights [E, N, K] -> the MMA-tiled layout (same shape and
+    dtype; opaque order) for Experts(..., tiled=True)."""
+    E, N, K = w.shape
+    out = torch.empty_like(w)
+    _check("moe_pack_bf16", native().moe_pack_bf16(
+        E, N, K, _ptr(w, torch.bfloat16, (E, N, K), "w"), _ptr(out, torch.bfloat16, (E, N, K), "out"),
+        _stream(stream)))
+    return out
 
 
 def moe_permute_noalloc(d: MoeDims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src,

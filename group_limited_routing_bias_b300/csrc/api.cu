@@ -116,6 +116,8 @@ bool ptrs_ok(std::initializer_list<const void *> ps) {
 
 moe_status check_experts(const moe_dims *d, const moe_experts *ex) {
   if (!ex) return MOE_ERR_INVALID_ARG;
+  if (ex->layout != MOE_LAYOUT_ROWMAJOR && ex->layout != MOE_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
+  if (ex->layout == MOE_LAYOUT_TILED && ex->dtype != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
   if (ex->dtype == MOE_W_BF16) {
     if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down})) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -305,6 +307,13 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
                         at<__nv_bfloat16>(ws, L.h), status, s);
   if (st != MOE_OK) return st;
   return launch_combine(d, y_partial, slot_of, y, s);
+}
+
+moe_status moe_pack_bf16(int E, int N, int K, const void *src, void *dst, moe_stream_t stream) {
+  if (E < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if ((size_t)E * N * K == 0) return MOE_OK;
+  if (!ptrs_ok({src, dst}) || src == dst) return MOE_ERR_INVALID_ARG;
+  return launch_pack_bf16(E, N, K, src, dst, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_quantize_nvfp4(int rows, int cols, const void *x, float g, uint8_t *q, uint8_t *s,

@@ -58,6 +58,10 @@ struct ExpertGemm {
     __nv_bfloat16 *out;  // h [Tk, I] or y_partial [Tk, H]
     int E, out_cols, a_rows, ksteps, mt;
     uint32_t *status;
+    // MMA-tiled weights (moe_pack_bf16), or null: each 128 x 64 tile is one
+    // contiguous 16 KB copy instead of a 2-D TMA box
+    const uint8_t *wp0, *wp1;
+    int ktiles;  // 64-wide k blocks per weight row
   };
   using Sched = ExpertSched;
   struct Tile {
@@ -113,10 +117,16 @@ struct ExpertGemm {
 #pragma unroll
     for (int sub = 0; sub < KSUB; ++sub) {
       uint8_t *st = stage + sub * StageGeom<BN, NA>::kBytes;
-      const int kx = (k * KSUB + sub) * kTileK;
-      tma_load_2d(st, &p.tmap_a0, bar, kx, t.arow0);
-      if (GATEUP) tma_load_2d(st + kATileBytes, &p.tmap_a1, bar, kx, t.arow0);
-      tma_load_2d(st + NA * kATileBytes, &p.tmap_b, bar, kx, t.row0);
+      const int kb = k * KSUB + sub;
+      if (p.wp0) {
+        const size_t tile = (size_t)(t.arow0 / kTileM) * p.ktiles + kb;
+        bulk_load(st, p.wp0 + tile * kATileBytes, kATileBytes, bar);
+        if (GATEUP) bulk_load(st + kATileBytes, p.wp1 + tile * kATileBytes, kATileBytes, bar);
+      } else {
+        tma_load_2d(st, &p.tmap_a0, bar, kb * kTileK, t.arow0);
+        if (GATEUP) tma_load_2d(st + kATileBytes, &p.tmap_a1, bar, kb * kTileK, t.arow0);
+      }
+      tma_load_2d(st + NA * kATileBytes, &p.tmap_b, bar, kb * kTileK, t.row0);
     }
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
@@ -190,6 +200,8 @@ struct ExpertGemmTM {
     __nv_bfloat16 *out;  // h [Tk, I] or y_partial [Tk, H]
     int E, out_cols, b_rows, ksteps, nf;
     uint32_t *status;
+    const uint8_t *wp0, *wp1;  // MMA-tiled weights (moe_pack_bf16), or null
+    int ktiles;                // 64-wide k blocks per weight row
   };
   using Sched = TokenMajorSched;
   struct Tile {
@@ -245,7 +257,14 @@ struct ExpertGemmTM {
   __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
     tma_load_2d(stage, &p.tmap_a, bar, k * kTileK, t.row0);
-    if (GATEUP) {
+    if (p.wp0) {  // 16 KB tiles: gate then up, or two 128-row blocks of W_down
+      const size_t t0 = (size_t)(t.brow0 / kTileM) * p.ktiles + k;
+      bulk_load(stage + kATileBytes, p.wp0 + t0 * kATileBytes, kATileBytes, bar);
+      if (GATEUP)
+        bulk_load(stage + 2 * kATileBytes, p.wp1 + t0 * kATileBytes, kATileBytes, bar);
+      else
+        bulk_load(stage + 2 * kATileBytes, p.wp0 + (t0 + p.ktiles) * kATileBytes, kATileBytes, bar);
+    } else if (GATEUP) {
       tma_load_2d(stage + kATileBytes, &p.tmap_b0, bar, k * kTileK, t.brow0);
       tma_load_2d(stage + 2 * kATileBytes, &p.tmap_b1, bar, k * kTileK, t.brow0);
     } else {
@@ -336,6 +355,10 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     prm.ksteps = d.H / (kTileK * P::KSUB);
     prm.mt = d.I / kTileM;
     prm.status = status;
+    const bool tiled = ex.layout == MOE_LAYOUT_TILED;
+    prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_gate) : nullptr;
+    prm.wp1 = tiled ? static_cast<const uint8_t *>(ex.w_up) : nullptr;
+    prm.ktiles = d.H / kTileK;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
     const moe_status st = launch_gemm<P>(prm, grid, stream);
     if (st != MOE_OK) return st;
@@ -357,6 +380,10 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     prm.ksteps = d.I / (kTileK * P::KSUB);
     prm.mt = d.H / kTileM;
     prm.status = status;
+    const bool tiled = ex.layout == MOE_LAYOUT_TILED;
+    prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_down) : nullptr;
+    prm.wp1 = nullptr;
+    prm.ktiles = d.I / kTileK;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
     return launch_gemm<P>(prm, grid, stream);
   }
@@ -386,6 +413,10 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
     prm.ksteps = d.H / kTileK;
     prm.nf = d.I / P::FW;
     prm.status = status;
+    const bool tiled = ex.layout == MOE_LAYOUT_TILED;
+    prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_gate) : nullptr;
+    prm.wp1 = tiled ? static_cast<const uint8_t *>(ex.w_up) : nullptr;
+    prm.ktiles = d.H / kTileK;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.nf));
     const moe_status st = launch_gemm<P>(prm, grid, stream);
     if (st != MOE_OK) return st;
@@ -407,6 +438,10 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
     prm.ksteps = d.I / kTileK;
     prm.nf = d.H / P::FW;
     prm.status = status;
+    const bool tiled = ex.layout == MOE_LAYOUT_TILED;
+    prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_down) : nullptr;
+    prm.wp1 = nullptr;
+    prm.ktiles = d.I / kTileK;
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.nf));
     return launch_gemm<P>(prm, grid, stream);
   }

@@ -171,6 +171,9 @@ moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const vo
                               const float *topk_w, void *y_partial, void *h16, uint32_t *status,
                               cudaStream_t stream);
 
+// bf16 [E, N, K] -> MMA-tiled layout (see moe_pack_bf16 in beam_moe.h).
+moe_status launch_pack_bf16(int E, int N, int K, const void *src, void *dst, cudaStream_t stream);
+
 // n bf16 values -> f16 (n even).
 moe_status launch_bf16_to_f16(const void *in, void *out, size_t n, cudaStream_t stream);
 

@@ -125,7 +125,13 @@ typedef struct {
   float x_global, h_global;              /* MOE_W_NVFP4_A4 only: static fp32 global
                                             scales of the x and h quantisers (finite,
                                             > 0; see moe_quantize_nvfp4)            */
+  int layout;                            /* MOE_LAYOUT_ROWMAJOR, or MOE_LAYOUT_TILED
+                                            for bf16 weights packed by moe_pack_bf16 */
 } moe_experts;
+
+/* Layout of bf16 expert weights. */
+#define MOE_LAYOUT_ROWMAJOR 0 /* [E, N, K] as in the layouts above                */
+#define MOE_LAYOUT_TILED 1    /* the MMA-tiled layout written by moe_pack_bf16     */
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int moe_version(void);
@@ -247,6 +253,21 @@ moe_status moe_bias_update(const moe_dims *dims, const int32_t *topk_idx, float 
  */
 moe_status moe_quantize_nvfp4(int rows, int cols, const void *x, float g, uint8_t *q, uint8_t *s,
                               moe_stream_t stream);
+
+/*
+ * Packs one bf16 weight tensor [E, N, K] (row-major, K contiguous: W_gate or
+ * W_up with N = I, K = H; W_down with N = H, K = I) into the MMA-tiled layout
+ * that moe_experts.layout = MOE_LAYOUT_TILED expects: tiles of 128 rows x 64 k,
+ * each stored as the 16 KB image the expert GEMMs hold in shared memory (the
+ * 128-byte swizzle: 16-byte chunk c of row r at position c XOR (r mod 8) of the
+ * row), ordered expert, 128-row block, k block.  Same size as the source.  A
+ * tile then streams from HBM as one contiguous copy; results are bit for bit
+ * those of the row-major layout.  The pages give no weight layout (a
+ * load-time preparation step of this implementation, like the NVFP4 packing).
+ *   Needs N % 128 == 0, K % 64 == 0, src and dst distinct and 16-byte aligned.
+ *   Asynchronous on `stream`; needs no workspace.
+ */
+moe_status moe_pack_bf16(int E, int N, int K, const void *src, void *dst, moe_stream_t stream);
 
 /*
  * moe_permute_noalloc — the dispatch of moe_permute for callers that cannot
