@@ -109,10 +109,10 @@ struct Nvfp4Format {
     tma_load_2d(raw + NW * kPackedRowBytes + first_row * kScaleBoxBytes, s, bar,
                 (k >> 2) * kScaleBoxBytes, wrow);
   }
-  template <int NW>
+  template <int NW, int NTHR>
   __device__ static void convert(const uint8_t *raw, uint8_t *dst, int k, int ctid) {
 #pragma unroll
-    for (int it = ctid; it < 2 * NW; it += 32 * kConvertWarps) {
+    for (int it = ctid; it < 2 * NW; it += NTHR) {
       const int r = it >> 1, half = it & 1;
       const uint32_t sc = *reinterpret_cast<const uint16_t *>(
           raw + NW * kPackedRowBytes + r * kScaleBoxBytes + (k & 3) * 4 + half * 2);
@@ -130,10 +130,10 @@ struct Fp8Format {
                                    const CUtensorMap *, uint64_t *bar, int k, int wrow) {
     tma_load_2d(raw + first_row * kFp8RowBytes, q, bar, k * kFp8RowBytes, wrow);
   }
-  template <int NW>
+  template <int NW, int NTHR>
   __device__ static void convert(const uint8_t *raw, uint8_t *dst, int, int ctid) {
 #pragma unroll
-    for (int it = ctid; it < 2 * NW; it += 32 * kConvertWarps) {
+    for (int it = ctid; it < 2 * NW; it += NTHR) {
       const int r = it >> 1, half = it & 1;
       fp8_half_row_to_f16(raw + r * kFp8RowBytes + half * 32, dst + r * 128, r, half);
     }
@@ -226,7 +226,8 @@ struct ExpertGemmFP4 {
   }
   __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage,
                                  const uint8_t *raw, int ctid) {
-    Fmt::template convert<NW>(raw, stage, k, ctid);  // A tiles: gate rows 0..127, up rows 128..255
+    // A tiles: gate rows 0..127, up rows 128..255; all converter warps on one slice
+    Fmt::template convert<NW, 32 * kConvertWarps>(raw, stage, k, ctid);
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     constexpr int CH = BN < 32 ? BN : 32;
@@ -272,6 +273,7 @@ struct ExpertGemmTMFP4 {
   static constexpr int BN = 256;
   static constexpr int NA = 1;
   static constexpr int NW = 256;
+  static constexpr int CGROUPS = 2;  // two converter groups on alternate K slices
   static constexpr bool CONVERT = true;
   static constexpr bool F16 = true;
   static constexpr int RAW_BYTES = NW * Fmt::kRawRowBytes;
@@ -317,7 +319,8 @@ struct ExpertGemmTMFP4 {
   }
   __device__ static void convert(const Params &, const Tile &, int k, uint8_t *stage,
                                  const uint8_t *raw, int ctid) {
-    Fmt::template convert<NW>(raw, stage + kATileBytes, k, ctid);  // B tile: 256 weight rows
+    // B tile: 256 weight rows; each converter group converts its own slices
+    Fmt::template convert<NW, 32 * kConvertWarps / CGROUPS>(raw, stage + kATileBytes, k, ctid);
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     const bool valid = row < t.nrows;

@@ -14,10 +14,13 @@
 // Problems whose weights arrive packed (NVFP4) add a converter role and a
 // second ring: warp 0 TMA-loads the packed bytes of each K slice into a deep
 // raw ring (RSTAGES), warp 3 the activation tile into the operand ring;
-//   warps 8..15   : wait for a slice's raw bytes, dequantise them into the
-//                   operand slot's swizzled weight tile, release the raw slot
-//                   at once, fence the generic proxy against the tensor
-//                   cores' async proxy, then signal the MMA.
+//   warps 8..15   : P::CGROUPS groups (optional, default 1) taking alternate
+//                   K slices (two groups dequantise two slices at once; faster
+//                   for the large-batch tiles): wait for a slice's raw
+//                   bytes, dequantise them into the operand slot's swizzled
+//                   weight tile, release the raw slot at once, fence the
+//                   generic proxy against the tensor cores' async proxy, then
+//                   signal the MMA.
 // The raw ring is refilled as soon as a slice is converted, so the bytes in
 // flight are not held back by MMA completion.
 //
@@ -39,7 +42,7 @@
 //   raw ring with
 //   static void load_raw(const Params&, const Tile&, int k, uint8_t *raw, uint64_t *raw_bar)
 //   static void convert(const Params&, const Tile&, int k, uint8_t *stage, const uint8_t *raw,
-//                       int ctid)   (ctid 0..255)
+//                       int ctid)   (ctid: thread within its converter group)
 #pragma once
 
 #include <type_traits>
@@ -89,6 +92,16 @@ __host__ __device__ constexpr int smem_bytes_for() {
 
 constexpr int kConvertWarps = 8;
 
+// Converter groups taking alternate K slices (optional P::CGROUPS, default 1).
+template <class P, class = void>
+struct CGroupsOf {
+  static constexpr int value = 1;
+};
+template <class P>
+struct CGroupsOf<P, std::void_t<decltype(P::CGROUPS)>> {
+  static constexpr int value = P::CGROUPS;
+};
+
 template <class P>
 __host__ __device__ constexpr int threads_for() {
   return P::CONVERT ? 256 + 32 * kConvertWarps : 256;
@@ -106,6 +119,9 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   constexpr uint32_t kTmemCols = tmem_cols_pow2(P::NBUF * kAccCols);
   constexpr uint32_t kIdesc = P::F16 ? umma_idesc_f16(kTileM, P::BN) : umma_idesc_bf16(kTileM, P::BN);
   static_assert(P::NBUF * kAccCols <= 512, "accumulators exceed tensor memory");
+  constexpr int CG = CGroupsOf<P>::value;
+  constexpr int kGroupWarps = kConvertWarps / CG;
+  static_assert(kConvertWarps % CG == 0, "converter groups must split the converter warps");
   static_assert(KSubOf<P>::value == 1 || !P::CONVERT, "several K slices per stage: bf16 path only");
   static_assert(P::BN % 16 == 0 && P::BN >= 16 && P::BN <= 256, "invalid MMA N");
 
@@ -139,10 +155,10 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
-    for (int s = 0; s < P::STAGES; ++s) mbar_init(&ready[s], kConvertWarps);
+    for (int s = 0; s < P::STAGES; ++s) mbar_init(&ready[s], kGroupWarps);
     for (int s = 0; s < RS; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kConvertWarps);
+      mbar_init(&raw_empty[s], kGroupWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -269,29 +285,32 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
     }
   } else if (P::CONVERT && warp >= 8) {
     // ---------------- converters: raw packed weights -> swizzled operand tile
-    const int ctid = threadIdx.x - 256;
-    int stage = 0, rstage = 0;
+    const int group = CG == 1 ? 0 : (warp - 8) / kGroupWarps;
+    const int gtid = threadIdx.x - 256 - group * 32 * kGroupWarps;
+    int stage = 0, rstage = 0, n = 0;
     uint32_t ph = 0, rph = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       const typename P::Tile tile = P::tile(p, *sched, t);
       const int nk = P::num_k(p, tile);
-      for (int k = 0; k < nk; ++k) {
-        // the raw slice has landed, and the operand slot it goes to is free
-        bool got = mbar_wait(&raw_full[rstage], rph, abort_flag, p.status) &&
-                   mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status);
-        got = __all_sync(0xffffffffu, got);
-        if (!got) {
-          ok = false;
-          break;
+      for (int k = 0; k < nk; ++k, ++n) {
+        if (CG == 1 || n % CG == group) {
+          // the raw slice has landed, and the operand slot it goes to is free
+          bool got = mbar_wait(&raw_full[rstage], rph, abort_flag, p.status) &&
+                     mbar_wait(&empty[stage], ph ^ 1u, abort_flag, p.status);
+          got = __all_sync(0xffffffffu, got);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          if constexpr (P::CONVERT)
+            P::convert(p, tile, k, stages + stage * STAGE, raws + rstage * P::RAW_BYTES, gtid);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&raw_empty[rstage]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ready[stage]);
         }
-        if constexpr (P::CONVERT)
-          P::convert(p, tile, k, stages + stage * STAGE, raws + rstage * P::RAW_BYTES, ctid);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rstage]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ready[stage]);
         if (++rstage == RS) {
           rstage = 0;
           rph ^= 1u;
