@@ -122,6 +122,14 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   constexpr int CG = CGroupsOf<P>::value;
   constexpr int kGroupWarps = kConvertWarps / CG;
   static_assert(kConvertWarps % CG == 0, "converter groups must split the converter warps");
+  // Barrier waits go by phase parity, which is unambiguous only while a waiter
+  // is at most one phase behind.  A group reaching slice n must already know
+  // that slice n - RSTAGES (same raw slot) landed, and that the MMA of slice
+  // n - 2 STAGES (same operand slot, two uses back) completed: both hold when
+  // the earlier slice is the group's own (RSTAGES a multiple of the group
+  // count) and when its previous slice's wait covers it (STAGES >= groups).
+  static_assert(CG == 1 || (P::RSTAGES % CG == 0 && P::STAGES >= CG),
+                "converter groups need RSTAGES % groups == 0 and STAGES >= groups");
   static_assert(KSubOf<P>::value == 1 || !P::CONVERT, "several K slices per stage: bf16 path only");
   static_assert(P::BN % 16 == 0 && P::BN >= 16 && P::BN <= 256, "invalid MMA N");
 
