@@ -121,7 +121,7 @@ class ClockSampler:
 class Workload:
     """Seeded inputs of one workload resident on the GPU, plus buffers."""
 
-    def __init__(self, lib, cfg, weights, dev, stages=True, a4=None):
+    def __init__(self, lib, cfg, weights, dev, stages=True, a4=None, tiled=False):
         import moe_inputs as mi
         self.cfg = cfg
         self.d = lib.dims_of(cfg)
@@ -129,6 +129,8 @@ class Workload:
         self.x_host = x.pin_memory()
         self.x, self.wr, self.b = x.to(dev), wr.to(dev), b.to(dev)
         self.experts = lib.Experts(*weights, a4=a4)
+        if tiled:
+            self.experts = self.experts.to_tiled()
         self.wdtype = self.experts.dtype
         self.ws = lib.alloc_workspace(self.d, lib.MOE_OP_FORWARD, self.wdtype, device=dev)
         T, H, k, E = cfg.T, cfg.H, cfg.top_k, cfg.E
@@ -255,15 +257,16 @@ def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
     return out
 
 
-def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks, a4=None):
+def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks, a4=None, tiled=False):
     """Packed experts (NVFP4 or FP8): decode T=64 (HBM-bound: packed bytes of
     touched experts) and prefill T=16384 (W4A16 / W8A16: the bf16 tensor peak
     is its denominator; W4A4 (a4 given): the fp4 peak, the measured bf16 peak
-    times the nominal fp4/bf16 ratio 13.5/2.25)."""
-    out = {}
+    times the nominal fp4/bf16 ratio 13.5/2.25).  tiled: the weights in the
+    tiled layout of moe_pack_nvfp4 / moe_pack_fp8."""
+    out = {"layout": "tiled" if tiled else "row-major"}
     for name, T, steps in (("decode", 64, 50), ("prefill", 16384, 5)):
         cfg = mi.CONFIGS[fmt].with_T(T)
-        wl = Workload(lib, cfg, wts, dev, a4=a4)
+        wl = Workload(lib, cfg, wts, dev, a4=a4, tiled=tiled)
         for _ in range(3):
             wl.forward(lib)
         torch.cuda.synchronize()
@@ -431,14 +434,14 @@ def run_profile(args):
         weights = tuple(p[0] for p in packed) + (None, None, None) + tuple(p[1] for p in packed)
         torch.cuda.empty_cache()
     a4 = (mi.A4_X_GLOBAL, mi.A4_H_GLOBAL) if args.profile.startswith("w4a4-") else None
-    wl = Workload(lib, cfg, weights, dev, stages=False, a4=a4)
+    wl = Workload(lib, cfg, weights, dev, stages=False, a4=a4, tiled=args.tiled)
     for _ in range(args.warmup):
         wl.forward(lib)
     torch.cuda.synchronize()
     per = time_steps(lambda: wl.forward(lib), args.steps, lambda: None)
     assert lib.workspace_status(wl.ws) == 0
     print(json.dumps({"profile": args.profile, "T": cfg.T, "E": cfg.E, "steps": args.steps,
-                      "ms_per_step": statistics.mean(per)}))
+                      "tiled": args.tiled, "ms_per_step": statistics.mean(per)}))
 
 
 def launches_per_forward(T: int, top_k: int) -> int:
@@ -465,6 +468,8 @@ def main():
                                           "fp8-decode", "w4a4-decode", "w4a4-prefill",
                                           "w4a4-decode-small", "w4a4-prefill-small"], default=None,
                     help="run only warm-up + steps forwards of one workload (for ncu)")
+    ap.add_argument("--tiled", action="store_true",
+                    help="with --profile: expert weights in the tiled layout (moe_pack_*)")
     args = ap.parse_args()
     peaks = load_peaks()
     if args.profile:
@@ -562,14 +567,15 @@ def main():
     if not args.no_nvfp4:
         packed = [mi.quantize_experts_nvfp4(w) for w in weights]
         fp4w = tuple(p[0] for p in packed) + tuple(p[1] for p in packed) + tuple(p[2] for p in packed)
-        nvfp4 = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks)
+        nvfp4 = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks,
+                               tiled=True)
         nvfp4["w4a4"] = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks,
                                        a4=(mi.A4_X_GLOBAL, mi.A4_H_GLOBAL))
         del packed, fp4w
         torch.cuda.empty_cache()
         packed = [mi.quantize_experts_fp8(w) for w in weights]
         fp8w = tuple(p[0] for p in packed) + (None, None, None) + tuple(p[1] for p in packed)
-        fp8 = packed_figures(lib, mi, "fp8", fp8w, FP8_EXPERT_BYTES, dev, flush, peaks)
+        fp8 = packed_figures(lib, mi, "fp8", fp8w, FP8_EXPERT_BYTES, dev, flush, peaks, tiled=True)
         del packed, fp8w
         torch.cuda.empty_cache()
 

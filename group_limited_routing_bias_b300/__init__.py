@@ -29,7 +29,8 @@ MOE_LAYOUT_ROWMAJOR, MOE_LAYOUT_TILED = 0, 1
 EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
             "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
             "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_bias_update",
-            "moe_quantize_nvfp4", "moe_pack_bf16", "moe_permute_noalloc")
+            "moe_quantize_nvfp4", "moe_pack_bf16", "moe_pack_nvfp4", "moe_pack_fp8",
+            "moe_permute_noalloc")
 
 
 class MoeDims(ctypes.Structure):
@@ -63,6 +64,8 @@ _sig = {
     "moe_forward": ([_DP, _P, _P, _P, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _S, _P], _I),
     "moe_quantize_nvfp4": ([_I, _I, _P, ctypes.c_float, _P, _P, _P], _I),
     "moe_pack_bf16": ([_I, _I, _I, _P, _P, _P], _I),
+    "moe_pack_nvfp4": ([_I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_pack_fp8": ([_I, _I, _I, _P, _P, _P], _I),
     "moe_bias_update": ([_DP, _P, _P, ctypes.c_double, _I, _I, ctypes.POINTER(ctypes.c_float), _P], _I),
     "moe_permute_noalloc": ([_DP, _P, _P, _P, _P, _P, _P, _P], _I),
 }
@@ -173,7 +176,11 @@ class Experts:
     FP8: w_* e4m3 uint8 [E, N, K], s_* None, g_* fp32 [E, N] row scales.
     a4 = (x_global, h_global) with NVFP4 weights selects W4A4: x and h are
     quantised to NVFP4 with those static global scales.
-    tiled = True: bf16 weights packed by moe_pack_bf16 (the MMA-tiled layout).
+    tiled = True: weights in the tiled layouts of moe_pack_bf16 (bf16, same
+    shapes), moe_pack_nvfp4 (NVFP4: w_* uint8 [E, N, 9K/16] holding codes and
+    block scales, s_* None, wdtype = MOE_W_NVFP4) or moe_pack_fp8 (FP8, same
+    shapes); to_tiled() makes such a copy.  wdtype overrides the format that
+    the tensors' dtypes imply (needed only for tiled NVFP4).
     """
     w_gate: torch.Tensor
     w_up: torch.Tensor
@@ -186,17 +193,39 @@ class Experts:
     g_down: Optional[torch.Tensor] = None
     a4: Optional[tuple] = None
     tiled: bool = False
+    wdtype: Optional[int] = None
 
     @property
     def dtype(self) -> int:
+        if self.wdtype is not None:
+            return self.wdtype
         if self.w_gate.dtype != torch.uint8:
             return MOE_W_BF16
         if self.s_gate is None:
             return MOE_W_FP8
         return MOE_W_NVFP4 if self.a4 is None else MOE_W_NVFP4_A4
 
+    def to_tiled(self, stream=None) -> "Experts":
+        """A copy with the weights packed into the tiled layout (bf16, NVFP4
+        W4A16 or FP8; W4A4 takes row-major weights only)."""
+        if self.tiled:
+            return self
+        if self.dtype == MOE_W_BF16:
+            return Experts(*(moe_pack_bf16(w, stream) for w in (self.w_gate, self.w_up, self.w_down)),
+                           tiled=True)
+        if self.dtype == MOE_W_FP8:
+            return Experts(*(moe_pack_fp8(w, stream) for w in (self.w_gate, self.w_up, self.w_down)),
+                           None, None, None, self.g_gate, self.g_up, self.g_down, tiled=True)
+        if self.dtype == MOE_W_NVFP4:
+            return Experts(moe_pack_nvfp4(self.w_gate, self.s_gate, stream),
+                           moe_pack_nvfp4(self.w_up, self.s_up, stream),
+                           moe_pack_nvfp4(self.w_down, self.s_down, stream), None, None, None,
+                           self.g_gate, self.g_up, self.g_down, tiled=True, wdtype=MOE_W_NVFP4)
+        raise ValueError("W4A4 experts take row-major weights only")
+
     def struct(self, d: MoeDims) -> MoeExperts:
         E, H, I = d.E, d.H, d.I
+        layout = MOE_LAYOUT_TILED if self.tiled else MOE_LAYOUT_ROWMAJOR
         if self.dtype == MOE_W_BF16:
             bf = torch.bfloat16
             return MoeExperts(MOE_W_BF16, _ptr(self.w_gate, bf, (E, I, H), "w_gate"),
@@ -211,7 +240,14 @@ class Experts:
                               _ptr(self.w_down, u8, (E, H, I), "w_down"), None, None, None,
                               _ptr(self.g_gate, f32, (E, I), "g_gate"),
                               _ptr(self.g_up, f32, (E, I), "g_up"),
-                              _ptr(self.g_down, f32, (E, H), "g_down"))
+                              _ptr(self.g_down, f32, (E, H), "g_down"), 0.0, 0.0, layout)
+        if self.dtype == MOE_W_NVFP4 and self.tiled:
+            return MoeExperts(MOE_W_NVFP4,
+                              _ptr(self.w_gate, u8, (E, I, H * 9 // 16), "w_gate"),
+                              _ptr(self.w_up, u8, (E, I, H * 9 // 16), "w_up"),
+                              _ptr(self.w_down, u8, (E, H, I * 9 // 16), "w_down"), None, None, None,
+                              _ptr(self.g_gate, f32, (E,), "g_gate"), _ptr(self.g_up, f32, (E,), "g_up"),
+                              _ptr(self.g_down, f32, (E,), "g_down"), 0.0, 0.0, layout)
         gx, gh = self.a4 if self.a4 is not None else (0.0, 0.0)
         return MoeExperts(self.dtype,
                           _ptr(self.w_gate, u8, (E, I, H // 2), "w_gate"),
@@ -221,7 +257,7 @@ class Experts:
                           _ptr(self.s_up, u8, (E, I, H // 16), "s_up"),
                           _ptr(self.s_down, u8, (E, H, I // 16), "s_down"),
                           _ptr(self.g_gate, f32, (E,), "g_gate"), _ptr(self.g_up, f32, (E,), "g_up"),
-                          _ptr(self.g_down, f32, (E,), "g_down"), float(gx), float(gh))
+                          _ptr(self.g_down, f32, (E,), "g_down"), float(gx), float(gh), layout)
 
 
 def moe_route(d: MoeDims, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
@@ -310,6 +346,30 @@ def moe_pack_bf16(w: torch.Tensor, stream=None) -> torch.Tensor:
     out = torch.empty_like(w)
     _check("moe_pack_bf16", native().moe_pack_bf16(
         E, N, K, _ptr(w, torch.bfloat16, (E, N, K), "w"), _ptr(out, torch.bfloat16, (E, N, K), "out"),
+        _stream(stream)))
+    return out
+
+
+def moe_pack_nvfp4(q: torch.Tensor, s: torch.Tensor, stream=None) -> torch.Tensor:
+    """NVFP4 expert weights (codes q uint8 [E, N, K/2], scales s uint8
+    [E, N, K/16]) -> the tiled layout, uint8 [E, N, 9K/16] (opaque order),
+    for Experts(..., tiled=True, wdtype=MOE_W_NVFP4)."""
+    E, N, K2 = q.shape
+    K = 2 * K2
+    out = torch.empty(E, N, K * 9 // 16, dtype=torch.uint8, device=q.device)
+    _check("moe_pack_nvfp4", native().moe_pack_nvfp4(
+        E, N, K, _ptr(q, torch.uint8, (E, N, K // 2), "q"), _ptr(s, torch.uint8, (E, N, K // 16), "s"),
+        _ptr(out, torch.uint8, (E, N, K * 9 // 16), "out"), _stream(stream)))
+    return out
+
+
+def moe_pack_fp8(q: torch.Tensor, stream=None) -> torch.Tensor:
+    """FP8 expert weights (e4m3 codes uint8 [E, N, K]) -> the tiled layout
+    (same shape; opaque order) for Experts(..., tiled=True)."""
+    E, N, K = q.shape
+    out = torch.empty_like(q)
+    _check("moe_pack_fp8", native().moe_pack_fp8(
+        E, N, K, _ptr(q, torch.uint8, (E, N, K), "q"), _ptr(out, torch.uint8, (E, N, K), "out"),
         _stream(stream)))
     return out
 

@@ -117,14 +117,15 @@ bool ptrs_ok(std::initializer_list<const void *> ps) {
 moe_status check_experts(const moe_dims *d, const moe_experts *ex) {
   if (!ex) return MOE_ERR_INVALID_ARG;
   if (ex->layout != MOE_LAYOUT_ROWMAJOR && ex->layout != MOE_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
-  if (ex->layout == MOE_LAYOUT_TILED && ex->dtype != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool tiled = ex->layout == MOE_LAYOUT_TILED;
+  if (tiled && ex->dtype == MOE_W_NVFP4_A4) return MOE_ERR_UNSUPPORTED;
   if (ex->dtype == MOE_W_BF16) {
     if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down})) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
   }
   if (ex->dtype == MOE_W_NVFP4 || ex->dtype == MOE_W_NVFP4_A4) {
-    if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down, ex->s_gate, ex->s_up, ex->s_down}))
-      return MOE_ERR_INVALID_ARG;
+    if (!ptrs_ok({ex->w_gate, ex->w_up, ex->w_down})) return MOE_ERR_INVALID_ARG;
+    if (!tiled && !ptrs_ok({ex->s_gate, ex->s_up, ex->s_down})) return MOE_ERR_INVALID_ARG;
     if (ex->dtype == MOE_W_NVFP4_A4 &&
         !(finite_positive(ex->x_global) && finite_positive(ex->h_global)))
       return MOE_ERR_INVALID_ARG;
@@ -314,6 +315,21 @@ moe_status moe_pack_bf16(int E, int N, int K, const void *src, void *dst, moe_st
   if ((size_t)E * N * K == 0) return MOE_OK;
   if (!ptrs_ok({src, dst}) || src == dst) return MOE_ERR_INVALID_ARG;
   return launch_pack_bf16(E, N, K, src, dst, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_pack_nvfp4(int E, int N, int K, const uint8_t *q, const uint8_t *s, uint8_t *dst,
+                          moe_stream_t stream) {
+  if (E < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if ((size_t)E * N * K == 0) return MOE_OK;
+  if (!ptrs_ok({q, s, dst}) || dst == q || dst == s) return MOE_ERR_INVALID_ARG;
+  return launch_pack_nvfp4(E, N, K, q, s, dst, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_pack_fp8(int E, int N, int K, const uint8_t *q, uint8_t *dst, moe_stream_t stream) {
+  if (E < 0 || N < 0 || K < 0 || N % 128 != 0 || K % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if ((size_t)E * N * K == 0) return MOE_OK;
+  if (!ptrs_ok({q, dst}) || dst == q) return MOE_ERR_INVALID_ARG;
+  return launch_pack_fp8(E, N, K, q, dst, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_quantize_nvfp4(int rows, int cols, const void *x, float g, uint8_t *q, uint8_t *s,

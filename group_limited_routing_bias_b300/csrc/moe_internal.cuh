@@ -174,6 +174,12 @@ moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const vo
 // bf16 [E, N, K] -> MMA-tiled layout (see moe_pack_bf16 in beam_moe.h).
 moe_status launch_pack_bf16(int E, int N, int K, const void *src, void *dst, cudaStream_t stream);
 
+// NVFP4 codes [E, N, K/2] + scales [E, N, K/16], or FP8 codes [E, N, K] -> the
+// tiled layouts (see moe_pack_nvfp4 / moe_pack_fp8 in beam_moe.h).
+moe_status launch_pack_nvfp4(int E, int N, int K, const uint8_t *q, const uint8_t *s, uint8_t *dst,
+                             cudaStream_t stream);
+moe_status launch_pack_fp8(int E, int N, int K, const uint8_t *q, uint8_t *dst, cudaStream_t stream);
+
 // n bf16 values -> f16 (n even).
 moe_status launch_bf16_to_f16(const void *in, void *out, size_t n, cudaStream_t stream);
 

@@ -14,7 +14,8 @@
 // Problems whose weights arrive packed (NVFP4) add a converter role and a
 // second ring: warp 0 TMA-loads the packed bytes of each K slice into a deep
 // raw ring (RSTAGES), warp 3 the activation tile into the operand ring;
-//   warps 8..15   : P::CGROUPS groups (optional, default 1) taking alternate
+//   warps 8..     : P::CONVERT_WARPS converter warps (optional, default 8) in
+//                   P::CGROUPS groups (optional, default 1) taking alternate
 //                   K slices (two groups dequantise two slices at once; faster
 //                   for the large-batch tiles): wait for a slice's raw
 //                   bytes, dequantise them into the operand slot's swizzled
@@ -102,9 +103,19 @@ struct CGroupsOf<P, std::void_t<decltype(P::CGROUPS)>> {
   static constexpr int value = P::CGROUPS;
 };
 
+// Converter warps (optional P::CONVERT_WARPS, default kConvertWarps).
+template <class P, class = void>
+struct ConvertWarpsOf {
+  static constexpr int value = kConvertWarps;
+};
+template <class P>
+struct ConvertWarpsOf<P, std::void_t<decltype(P::CONVERT_WARPS)>> {
+  static constexpr int value = P::CONVERT_WARPS;
+};
+
 template <class P>
 __host__ __device__ constexpr int threads_for() {
-  return P::CONVERT ? 256 + 32 * kConvertWarps : 256;
+  return P::CONVERT ? 256 + 32 * ConvertWarpsOf<P>::value : 256;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -120,8 +131,8 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   constexpr uint32_t kIdesc = P::F16 ? umma_idesc_f16(kTileM, P::BN) : umma_idesc_bf16(kTileM, P::BN);
   static_assert(P::NBUF * kAccCols <= 512, "accumulators exceed tensor memory");
   constexpr int CG = CGroupsOf<P>::value;
-  constexpr int kGroupWarps = kConvertWarps / CG;
-  static_assert(kConvertWarps % CG == 0, "converter groups must split the converter warps");
+  constexpr int kGroupWarps = ConvertWarpsOf<P>::value / CG;
+  static_assert(ConvertWarpsOf<P>::value % CG == 0, "converter groups must split the converter warps");
   // Barrier waits go by phase parity, which is unambiguous only while a waiter
   // is at most one phase behind.  A group reaching slice n must already know
   // that slice n - RSTAGES (same raw slot) landed, and that the MMA of slice

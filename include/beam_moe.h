@@ -126,12 +126,17 @@ typedef struct {
                                             scales of the x and h quantisers (finite,
                                             > 0; see moe_quantize_nvfp4)            */
   int layout;                            /* MOE_LAYOUT_ROWMAJOR, or MOE_LAYOUT_TILED
-                                            for bf16 weights packed by moe_pack_bf16 */
+                                            for weights packed by moe_pack_bf16,
+                                            moe_pack_nvfp4 or moe_pack_fp8          */
 } moe_experts;
 
-/* Layout of bf16 expert weights. */
+/* Layout of the expert weights.  MOE_LAYOUT_TILED applies to MOE_W_BF16
+ * (w_* written by moe_pack_bf16), MOE_W_NVFP4 (w_* written by moe_pack_nvfp4,
+ * which holds the block scales too: s_* are then unused and may be NULL) and
+ * MOE_W_FP8 (w_* written by moe_pack_fp8; g_* as for row-major).  MOE_W_NVFP4_A4
+ * takes row-major weights only (MOE_ERR_UNSUPPORTED otherwise). */
 #define MOE_LAYOUT_ROWMAJOR 0 /* [E, N, K] as in the layouts above                */
-#define MOE_LAYOUT_TILED 1    /* the MMA-tiled layout written by moe_pack_bf16     */
+#define MOE_LAYOUT_TILED 1    /* the tiled layouts written by the moe_pack_* calls */
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int moe_version(void);
@@ -268,6 +273,35 @@ moe_status moe_quantize_nvfp4(int rows, int cols, const void *x, float g, uint8_
  *   Asynchronous on `stream`; needs no workspace.
  */
 moe_status moe_pack_bf16(int E, int N, int K, const void *src, void *dst, moe_stream_t stream);
+
+/*
+ * Packs one NVFP4 weight tensor (codes q uint8 [E, N, K/2], even k in the low
+ * nibble, and e4m3 block scales s uint8 [E, N, K/16], as in the NVFP4 layout
+ * above) into the tiled layout that moe_experts.layout = MOE_LAYOUT_TILED
+ * expects for MOE_W_NVFP4: tiles of 128 rows x 64 k, ordered expert, 128-row
+ * block, k block; a tile is 4608 bytes, the 128 rows' codes (32 bytes per row,
+ * row after row) followed by their scales (4 bytes per row, row after row).
+ * dst holds E * N * K * 9 / 16 bytes.  Each tile then streams from HBM as one
+ * contiguous copy instead of 256 short row segments; results are bit for bit
+ * those of the row-major layout.  A load-time preparation step of this
+ * implementation (the pages give no weight layout).
+ *   Needs N % 128 == 0, K % 64 == 0, all pointers 16-byte aligned, dst
+ *   distinct from q and s.  Asynchronous on `stream`; needs no workspace.
+ */
+moe_status moe_pack_nvfp4(int E, int N, int K, const uint8_t *q, const uint8_t *s, uint8_t *dst,
+                          moe_stream_t stream);
+
+/*
+ * Packs one FP8 weight tensor (e4m3 codes uint8 [E, N, K]) into the tiled
+ * layout that moe_experts.layout = MOE_LAYOUT_TILED expects for MOE_W_FP8:
+ * tiles of 128 rows x 64 k (8192 bytes, 64 bytes per row, row after row),
+ * ordered expert, 128-row block, k block.  dst holds E * N * K bytes; the row
+ * scales g_* keep their [E, N] layout.  Results are bit for bit those of the
+ * row-major layout.
+ *   Needs N % 128 == 0, K % 64 == 0, q and dst 16-byte aligned and distinct.
+ *   Asynchronous on `stream`; needs no workspace.
+ */
+moe_status moe_pack_fp8(int E, int N, int K, const uint8_t *q, uint8_t *dst, moe_stream_t stream);
 
 /*
  * moe_permute_noalloc — the dispatch of moe_permute for callers that cannot

@@ -21,7 +21,8 @@ def lib():
 
 
 class Fp8Case:
-    def __init__(self, cfg, T=None, seed=0):
+    def __init__(self, cfg, T=None, seed=0, tiled=False):
+        self.tiled, self._tiled_experts = tiled, None
         self.cfg = cfg if T is None else cfg.with_T(T)
         c = self.cfg
         x, wr, b = mi.make_router_inputs(c, seed=seed)
@@ -32,7 +33,12 @@ class Fp8Case:
         torch.cuda.empty_cache()
 
     def experts(self, lib):
-        return lib.Experts(self.qg, self.qu, self.qd, None, None, None, self.rg, self.ru, self.rd)
+        ex = lib.Experts(self.qg, self.qu, self.qd, None, None, None, self.rg, self.ru, self.rd)
+        if not self.tiled:
+            return ex
+        if self._tiled_experts is None:
+            self._tiled_experts = ex.to_tiled()
+        return self._tiled_experts
 
     def get_expert(self, e):
         M = oracle.Fp8Matrix
@@ -66,7 +72,7 @@ def check(lib, case, sample=None):
 
 @pytest.mark.parametrize("T", [64, 1, 300, 2048])
 def test_fp8_tiny(lib, T):
-    """T=2048 takes the token-major GEMMs (256 rows per expert on average)."""
+    """T=1 (4 rows) takes the weights-on-M GEMMs, the others the token-major ones."""
     check(lib, Fp8Case(mi.CONFIGS["tiny"], T=T))
 
 
@@ -76,3 +82,16 @@ def test_fp8_beam(lib, T, n_sample):
     sample = None if n_sample is None else np.sort(
         np.random.default_rng(T).choice(T, n_sample, replace=False))
     check(lib, case, sample)
+
+
+@pytest.mark.parametrize("name,T,n_sample", [("tiny", 5, None), ("tiny", 64, None), ("tiny", 2048, None),
+                                              ("fp8", 64, None), ("fp8", 16384, 48)])
+def test_fp8_tiled(lib, name, T, n_sample):
+    """Weights in the tiled layout (moe_pack_fp8), on both GEMM paths: parity
+    with the oracle, and the row-major forward's output bit for bit."""
+    case = Fp8Case(mi.CONFIGS[name], T=T)
+    sample = None if n_sample is None else np.sort(
+        np.random.default_rng(T).choice(T, n_sample, replace=False))
+    y_rm = check(lib, case, sample)
+    case.tiled = True
+    assert torch.equal(check(lib, case, sample), y_rm)

@@ -30,7 +30,8 @@ def lib():
 
 
 class Fp4Case:
-    def __init__(self, cfg, T=None, seed=0):
+    def __init__(self, cfg, T=None, seed=0, tiled=False):
+        self.tiled, self._tiled_experts = tiled, None
         self.cfg = cfg if T is None else cfg.with_T(T)
         c = self.cfg
         x, wr, b = mi.make_router_inputs(c, seed=seed)
@@ -44,8 +45,13 @@ class Fp4Case:
         torch.cuda.empty_cache()
 
     def experts(self, lib):
-        return lib.Experts(self.qg, self.qu, self.qd, self.sg, self.su, self.sd, self.gg, self.gu,
-                           self.gd)
+        ex = lib.Experts(self.qg, self.qu, self.qd, self.sg, self.su, self.sd, self.gg, self.gu,
+                         self.gd)
+        if not self.tiled:
+            return ex
+        if self._tiled_experts is None:
+            self._tiled_experts = ex.to_tiled()
+        return self._tiled_experts
 
     def get_expert(self, e):
         M = oracle.Nvfp4Matrix
@@ -85,7 +91,7 @@ def check(lib, case, sample=None):
 
 @pytest.mark.parametrize("T", [64, 200, 1, 2048])
 def test_nvfp4_tiny(lib, T):
-    """T=2048 gives 256 rows per expert: the token-major NVFP4 GEMMs."""
+    """T=1 (4 rows) takes the weights-on-M GEMMs, the others the token-major ones."""
     check(lib, Fp4Case(TINY4, T=T))
 
 
@@ -98,11 +104,33 @@ def test_nvfp4_beam(lib, T, n_sample):
     check(lib, case, sample)
 
 
-def test_nvfp4_experts_entry_point_matches_forward(lib):
+@pytest.mark.parametrize("T", [5, 64, 2048])
+def test_nvfp4_tiny_tiled(lib, T):
+    """Weights in the tiled layout (moe_pack_nvfp4), on both GEMM paths: parity
+    with the oracle, and the row-major forward's output bit for bit."""
+    case = Fp4Case(TINY4, T=T)
+    y_rm = check(lib, case)
+    case.tiled = True
+    assert torch.equal(check(lib, case), y_rm)
+
+
+@pytest.mark.parametrize("T,n_sample", [(1, None), (64, None), (16384, 48)])
+def test_nvfp4_beam_tiled(lib, T, n_sample):
+    case = Fp4Case(mi.CONFIGS["nvfp4"], T=T)
+    sample = None
+    if n_sample is not None:
+        sample = np.sort(np.random.default_rng(T).choice(T, n_sample, replace=False))
+    y_rm = check(lib, case, sample)
+    case.tiled = True
+    assert torch.equal(check(lib, case, sample), y_rm)
+
+
+@pytest.mark.parametrize("tiled", [False, True])
+def test_nvfp4_experts_entry_point_matches_forward(lib, tiled):
     """moe_experts_swiglu with NVFP4 weights (bf16 x_perm converted inside)
     gives the same y as moe_forward, bit for bit."""
     c = TINY4.with_T(300)
-    case = Fp4Case(c)
+    case = Fp4Case(c, tiled=tiled)
     d = lib.dims_of(c)
     y_fwd, _, _ = forward(lib, case)
     Tk = c.T * c.top_k

@@ -184,10 +184,10 @@ def check_forward(lib, case, sample=None):
     return y, idx, w
 
 
-@pytest.mark.parametrize("T", [64, 200, 1, 5, 1500, 2048])
+@pytest.mark.parametrize("T", [64, 200, 1, 5, 333, 1500, 2048])
 def test_forward_tiny(lib, T):
-    """Tiny shape; T >= 1500 gives >= 128 rows per expert on average, which takes
-    the token-major expert GEMMs (ragged expert tails included)."""
+    """Tiny shape; from T = 256 (1024 token rows at top-4) the token-major expert
+    GEMMs run (T = 333: ~42 rows per expert, every tile ragged)."""
     check_forward(lib, Case(mi.CONFIGS["tiny"], T=T))
 
 
@@ -206,6 +206,15 @@ def test_forward_tiny_skewed_token_major(lib):
 def test_forward_decode_full(lib):
     """The decode workload in the launch configuration the benchmark times."""
     check_forward(lib, Case(mi.CONFIGS["decode"]))
+
+
+@pytest.mark.parametrize("T", [256, 1024])
+def test_forward_beam_mid_batch_sampled(lib, T):
+    """Beam shape between decode and prefill: token-major tiles with a few to a
+    few dozen rows per expert."""
+    rng = np.random.default_rng(T)
+    case = Case(mi.CONFIGS["decode"], T=T)
+    check_forward(lib, case, sample=np.sort(rng.choice(T, 48, replace=False)))
 
 
 def test_forward_prefill_sampled(lib):
