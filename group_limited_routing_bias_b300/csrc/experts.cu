@@ -194,6 +194,7 @@ struct ExpertGemmTM {
 
   struct Params {
     CUtensorMap tmap_a;   // token rows [Tk, K]: x_perm or h, box {64, 128}
+    CUtensorMap tmap_a32, tmap_a64;  // the same rows, boxes {64, 32} and {64, 64}
     CUtensorMap tmap_b0;  // W_gate [E*I, H] box {64,128}, or W_down [E*H, I] box {64,256}
     CUtensorMap tmap_b1;  // W_up [E*I, H] box {64,128} (gate/up only)
     const int32_t *offsets;
@@ -213,7 +214,6 @@ struct ExpertGemmTM {
   static constexpr bool F16 = false;
   static constexpr int RAW_BYTES = 0;
   static constexpr int RSTAGES = 0;
-  static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 
   __device__ static void prologue(const Params &p, Sched &s) {
@@ -257,8 +257,13 @@ struct ExpertGemmTM {
     return Tile{row0, min(kTileM, s.off[e + 1] - row0), e * p.b_rows + f * FW, f};
   }
   __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
+  __device__ static uint32_t tx_bytes(const Params &, const Tile &t) {
+    return act_box_rows(t.nrows) * kTileK * 2 + 2 * kATileBytes;
+  }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
-    tma_load_2d(stage, &p.tmap_a, bar, k * kTileK, t.row0);
+    const int ar = act_box_rows(t.nrows);
+    tma_load_2d(stage, ar == 32 ? &p.tmap_a32 : ar == 64 ? &p.tmap_a64 : &p.tmap_a, bar, k * kTileK,
+                t.row0);
     if (p.wp0) {  // 16 KB tiles: gate then up, or two 128-row blocks of W_down
       const size_t t0 = (size_t)(t.brow0 / kTileM) * p.ktiles + k;
       bulk_load(stage + kATileBytes, p.wp0 + t0 * kATileBytes, kATileBytes, bar);
@@ -402,6 +407,8 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
     using P = ExpertGemmTM<true>;
     typename P::Params prm;
     if (!make_tmap_bf16_2d(&prm.tmap_a, x_perm, d.H, Tk, kTileM) ||
+        !make_tmap_bf16_2d(&prm.tmap_a32, x_perm, d.H, Tk, 32) ||
+        !make_tmap_bf16_2d(&prm.tmap_a64, x_perm, d.H, Tk, 64) ||
         !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_gate, d.H, (uint64_t)d.E * d.I, 128) ||
         !make_tmap_bf16_2d(&prm.tmap_b1, ex.w_up, d.H, (uint64_t)d.E * d.I, 128))
       return MOE_ERR_CUDA;
@@ -427,6 +434,8 @@ moe_status launch_experts_token_major(const moe_dims &d, const moe_experts &ex, 
     using P = ExpertGemmTM<false>;
     typename P::Params prm;
     if (!make_tmap_bf16_2d(&prm.tmap_a, h, d.I, Tk, kTileM) ||
+        !make_tmap_bf16_2d(&prm.tmap_a32, h, d.I, Tk, 32) ||
+        !make_tmap_bf16_2d(&prm.tmap_a64, h, d.I, Tk, 64) ||
         !make_tmap_bf16_2d(&prm.tmap_b0, ex.w_down, d.I, (uint64_t)d.E * d.H, 256))
       return MOE_ERR_CUDA;
     prm.tmap_b1 = prm.tmap_b0;

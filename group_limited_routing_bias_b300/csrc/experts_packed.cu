@@ -205,6 +205,7 @@ __device__ __forceinline__ void tmem_ld_n<16>(uint32_t taddr, uint32_t (&r)[16])
 
 struct Fp4Params {
   CUtensorMap tmap_act;  // f16 token rows [Tk, K] (x or h), 128-byte swizzle
+  CUtensorMap tmap_act32, tmap_act64;  // token-major tiles: the same rows, 32- and 64-row boxes
   CUtensorMap tmap_q0;   // packed codes [E*N, K/2] of W_gate or W_down
   CUtensorMap tmap_q1;   // packed codes of W_up (gate/up only)
   CUtensorMap tmap_s0;   // e4m3 scales [E*N, K/16] of W_gate or W_down
@@ -330,7 +331,6 @@ struct ExpertGemmTMFP4 {
   static constexpr bool CONVERT = true;
   static constexpr bool F16 = true;
   static constexpr int RAW_BYTES = NW * Fmt::kRawRowBytes;
-  static constexpr int TX_BYTES = kATileBytes;  // the activation tile; raw bytes on their own ring
   static constexpr int NBUF = 2;
   static constexpr int STAGES = 3;
   static constexpr int RSTAGES_FIT = (kSmemLimit - kSmemReserve - (int)sizeof(TileSched) -
@@ -358,8 +358,13 @@ struct ExpertGemmTMFP4 {
     return Tile{row0, min(kTileM, s.off[e + 1] - row0), e * p.w_rows + f * FW, f, e};
   }
   __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
+  __device__ static uint32_t tx_bytes(const Params &, const Tile &t) {
+    return act_box_rows(t.nrows) * kTileK * 2;
+  }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
-    tma_load_2d(stage, &p.tmap_act, bar, k * kTileK, t.row0);
+    const int ar = act_box_rows(t.nrows);
+    tma_load_2d(stage, ar == 32 ? &p.tmap_act32 : ar == 64 ? &p.tmap_act64 : &p.tmap_act, bar,
+                k * kTileK, t.row0);
   }
   __device__ static void load_raw(const Params &p, const Tile &t, int k, uint8_t *raw,
                                   uint64_t *raw_bar) {
@@ -566,6 +571,8 @@ moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const v
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.I;
     if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, kTileM) ||
+        !make_act_map(&prm.tmap_act32, x16, d.H, Tk, 32) ||
+        !make_act_map(&prm.tmap_act64, x16, d.H, Tk, 64) ||
         !set_weights<Fmt>(prm, ex.w_gate, ex.s_gate, ex.w_up, ex.s_up, d.H, rows, 128))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_gate;
@@ -585,6 +592,8 @@ moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const v
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.H;
     if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, kTileM) ||
+        !make_act_map(&prm.tmap_act32, h16, d.I, Tk, 32) ||
+        !make_act_map(&prm.tmap_act64, h16, d.I, Tk, 64) ||
         !set_weights<Fmt>(prm, ex.w_down, ex.s_down, ex.w_down, ex.s_down, d.I, rows, 256))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_down;

@@ -26,7 +26,7 @@
 // flight are not held back by MMA completion.
 //
 // A problem class P supplies the shapes and the tile schedule:
-//   static constexpr int BN, NA, STAGES, NBUF, TX_BYTES;
+//   static constexpr int BN, NA, STAGES, NBUF, TX_BYTES (or a tx_bytes hook, below);
 //   static constexpr bool CONVERT, F16;   (packed weights; f16 instead of bf16 operands)
 //   static constexpr int KSUB;            (optional, default 1: 64-wide K slices per stage;
 //                                          two let each weight row arrive as 256 contiguous
@@ -38,6 +38,8 @@
 //   static Tile tile(const Params&, const Sched&, int t)
 //   static int  num_k(const Params&, const Tile&)
 //   static void load(const Params&, const Tile&, int k, uint8_t *stage, uint64_t *bar)
+//   static uint32_t tx_bytes(const Params&, const Tile&)  (optional: the bytes load()
+//                                          brings for that tile, when not TX_BYTES)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
 //   CONVERT problems load the operand ring's activation tile with load() and the
 //   raw ring with
@@ -47,6 +49,7 @@
 #pragma once
 
 #include <type_traits>
+#include <utility>
 
 #include "ptx.cuh"
 
@@ -116,6 +119,26 @@ struct ConvertWarpsOf<P, std::void_t<decltype(P::CONVERT_WARPS)>> {
 template <class P>
 __host__ __device__ constexpr int threads_for() {
   return P::CONVERT ? 256 + 32 * ConvertWarpsOf<P>::value : 256;
+}
+
+template <class P, class = void>
+struct HasTxBytes : std::false_type {};
+template <class P>
+struct HasTxBytes<P, std::void_t<decltype(P::tx_bytes(std::declval<const typename P::Params &>(),
+                                                       std::declval<const typename P::Tile &>()))>>
+    : std::true_type {};
+
+template <class P>
+__device__ __forceinline__ uint32_t tx_bytes_of(const typename P::Params &p, const typename P::Tile &t) {
+  if constexpr (HasTxBytes<P>::value) return P::tx_bytes(p, t);
+  else return P::TX_BYTES;
+}
+
+// Token rows of the activation box that a token-major tile loads: the MMA
+// always reads 128 rows, but rows past the tile's own are never stored, so a
+// tile of a few rows loads a 32- or 64-row box and leaves the rest stale.
+__host__ __device__ constexpr int act_box_rows(int nrows) {
+  return nrows <= 32 ? 32 : nrows <= 64 ? 64 : 128;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(&full[stage], P::TX_BYTES);
+              mbar_arrive_expect_tx(&full[stage], tx_bytes_of<P>(p, tile));
               P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
             }
           } else {
@@ -229,7 +252,7 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], P::TX_BYTES);
+            mbar_arrive_expect_tx(&full[stage], tx_bytes_of<P>(p, tile));
             P::load(p, tile, k, stages + stage * STAGE, &full[stage]);
           }
           issued |= 1u << stage;
