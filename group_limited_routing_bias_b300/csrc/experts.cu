@@ -49,6 +49,7 @@ struct ExpertGemm {
       (kSmemLimit - kSmemReserve - (int)sizeof(ExpertSched)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
   static_assert(STAGES >= 2, "pipeline needs two stages");
+  static constexpr bool DYNAMIC = true;  // tiles taken from a global counter
 
   struct Params {
     CUtensorMap tmap_a0;  // weights [E * a_rows, K]: W_gate or W_down
@@ -64,6 +65,7 @@ struct ExpertGemm {
     // contiguous 16 KB copy instead of a 2-D TMA box
     const uint8_t *wp0, *wp1;
     int ktiles;  // 64-wide k blocks per weight row
+    uint32_t *sched_counters;  // dynamic tile schedule (workspace header)
   };
   using Sched = ExpertSched;
   struct Tile {
@@ -362,6 +364,7 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     prm.ksteps = d.H / (kTileK * P::KSUB);
     prm.mt = d.I / kTileM;
     prm.status = status;
+    prm.sched_counters = status + kSchedCounterWord;
     const bool tiled = ex.layout == MOE_LAYOUT_TILED;
     prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_gate) : nullptr;
     prm.wp1 = tiled ? static_cast<const uint8_t *>(ex.w_up) : nullptr;
@@ -387,6 +390,7 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     prm.ksteps = d.I / (kTileK * P::KSUB);
     prm.mt = d.H / kTileM;
     prm.status = status;
+    prm.sched_counters = status + kSchedCounterWord;
     const bool tiled = ex.layout == MOE_LAYOUT_TILED;
     prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_down) : nullptr;
     prm.wp1 = nullptr;

@@ -16,6 +16,10 @@ namespace beam {
 constexpr int kTargetCtas = 148;       // B300 SM count; sizes the router's K split
 constexpr int kPermuteChunk = 4096;    // entries per permute CTA (32 warps x 128)
 constexpr size_t kHeaderBytes = 256;   // workspace status header
+// Header layout (uint32 words): [0] the device status word; [32], [33] the
+// counters of the dynamic tile schedule (next tile, finished CTAs), zero
+// between launches.
+constexpr size_t kSchedCounterWord = 32;
 constexpr int kMaxRouterSplit = 20;    // router K split; the top-k kernel adds the partials
 
 inline int ilog2(int v) {

@@ -25,6 +25,15 @@
 // The raw ring is refilled as soon as a slice is converted, so the bytes in
 // flight are not held back by MMA completion.
 //
+// Tile schedule: by default CTA b takes tiles b, b + grid, b + 2 grid, ...
+// A problem with P::DYNAMIC (bf16 problems) instead has its producer take the
+// next tile from a global counter (P::Params::sched_counters[0]) as it starts
+// loading it, and hand the index to the MMA and epilogue roles through a
+// kTileRing-deep ring in shared memory, so SMs that stream faster take more
+// tiles and the tail shrinks.  The last CTA to finish zeroes both counters
+// (sched_counters[1] counts finished CTAs), so they start at zero for the next
+// launch; they must be zero before the first.
+//
 // A problem class P supplies the shapes and the tile schedule:
 //   static constexpr int BN, NA, STAGES, NBUF, TX_BYTES (or a tx_bytes hook, below);
 //   static constexpr bool CONVERT, F16;   (packed weights; f16 instead of bf16 operands)
@@ -116,6 +125,17 @@ struct ConvertWarpsOf<P, std::void_t<decltype(P::CONVERT_WARPS)>> {
   static constexpr int value = P::CONVERT_WARPS;
 };
 
+template <class P, class = void>
+struct DynamicOf {
+  static constexpr bool value = false;
+};
+template <class P>
+struct DynamicOf<P, std::void_t<decltype(P::DYNAMIC)>> {
+  static constexpr bool value = P::DYNAMIC;
+};
+
+constexpr int kTileRing = 4;
+
 template <class P>
 __host__ __device__ constexpr int threads_for() {
   return P::CONVERT ? 256 + 32 * ConvertWarpsOf<P>::value : 256;
@@ -166,6 +186,8 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
                 "converter groups need RSTAGES % groups == 0 and STAGES >= groups");
   static_assert(KSubOf<P>::value == 1 || !P::CONVERT, "several K slices per stage: bf16 path only");
   static_assert(P::BN % 16 == 0 && P::BN >= 16 && P::BN <= 256, "invalid MMA N");
+  constexpr bool DYN = DynamicOf<P>::value;
+  static_assert(!DYN || !P::CONVERT, "dynamic tile schedule: problems without converters only");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -180,8 +202,14 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   uint64_t *raw_full = ready + P::STAGES;
   uint64_t *raw_empty = raw_full + RS;
   uint64_t *drain = raw_empty + RS;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *tr_full = drain + 1;  // tile ring (DYNAMIC only)
+  uint64_t *tr_empty = tr_full + kTileRing;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tr_empty + kTileRing);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *tring = abort_flag + 1;
+  static_assert((3 * P::STAGES + 2 * P::NBUF + 2 * RS + 1 + 2 * kTileRing) * 8 + 8 +
+                        4 * kTileRing <= 1024,
+                "barrier area");
   typename P::Sched *sched = reinterpret_cast<typename P::Sched *>(
       raws + raw_ring_bytes_of<P>() + 1024);
 
@@ -203,6 +231,10 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       mbar_init(&raw_empty[s], kGroupWarps);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(&tr_full[s], 1);
+      mbar_init(&tr_empty[s], 1 + 4);  // the MMA thread and the four epilogue warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -217,6 +249,53 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   const uint32_t tmem_base = *tmem_slot;
   const int ntiles = P::num_tiles(p, *sched);
 
+  // Tile feed.  `cur` is the static cursor; slot / tph index the tile ring.
+  // The producer publishes each tile it takes (-1 at the end); consumers read
+  // them in order (whole_warp: every lane waits, lane 0 releases the slot).
+  auto produce_tile = [&](int &cur, int &slot, uint32_t &tph, bool &ok) -> int {
+    if constexpr (!DYN) {
+      const int t = cur;
+      cur += gridDim.x;
+      return t < ntiles ? t : -1;
+    } else {
+      int t = (int)atomicAdd(p.sched_counters, 1u);
+      if (t >= ntiles) t = -1;
+      if (!mbar_wait(&tr_empty[slot], tph ^ 1u, abort_flag, p.status)) {
+        ok = false;
+        return -1;
+      }
+      tring[slot] = t;
+      mbar_arrive(&tr_full[slot]);
+      if (++slot == kTileRing) {
+        slot = 0;
+        tph ^= 1u;
+      }
+      return t;
+    }
+  };
+  auto consume_tile = [&](int &cur, int &slot, uint32_t &tph, bool &ok, bool whole_warp) -> int {
+    if constexpr (!DYN) {
+      const int t = cur;
+      cur += gridDim.x;
+      return t < ntiles ? t : -1;
+    } else {
+      bool got = mbar_wait(&tr_full[slot], tph, abort_flag, p.status);
+      if (whole_warp) got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        return -1;
+      }
+      const int t = tring[slot];
+      if (whole_warp) __syncwarp();
+      if (!whole_warp || lane == 0) mbar_arrive(&tr_empty[slot]);
+      if (++slot == kTileRing) {
+        slot = 0;
+        tph ^= 1u;
+      }
+      return t;
+    }
+  };
+
   if (warp == 0 || (P::CONVERT && warp == 3)) {
     if (lane == 0) {
       // ---------------- TMA producers.  Without conversion warp 0 fills the
@@ -224,10 +303,11 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       // (gated only by the converters freeing raw slots) and warp 3 issues the
       // activation tiles into the operand ring (gated by MMA completion).
       const bool raw_role = P::CONVERT && warp == 0;
-      int stage = 0;
-      uint32_t ph = 0, issued = 0, par = 0;
+      int stage = 0, cur = blockIdx.x, tslot = 0;
+      uint32_t ph = 0, issued = 0, par = 0, tph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      for (int t = produce_tile(cur, tslot, tph, ok); ok && t >= 0;
+           t = produce_tile(cur, tslot, tph, ok)) {
         const typename P::Tile tile = P::tile(p, *sched, t);
         const int nk = P::num_k(p, tile);
         for (int k = 0; k < nk; ++k) {
@@ -272,10 +352,11 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      int stage = 0, buf = 0;
-      uint32_t ph = 0, bph = 0;
+      int stage = 0, buf = 0, cur = blockIdx.x, tslot = 0;
+      uint32_t ph = 0, bph = 0, tph = 0;
       bool ok = true, any = false;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      for (int t = consume_tile(cur, tslot, tph, ok, false); ok && t >= 0;
+           t = consume_tile(cur, tslot, tph, ok, false)) {
         const typename P::Tile tile = P::tile(p, *sched, t);
         const int nk = P::num_k(p, tile);
         if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, p.status)) {
@@ -367,9 +448,11 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
     // ---------------- epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    int buf = 0;
-    uint32_t bph = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    int buf = 0, cur = blockIdx.x, tslot = 0;
+    uint32_t bph = 0, tph = 0;
+    bool fed = true;
+    for (int t = consume_tile(cur, tslot, tph, fed, true); fed && t >= 0;
+         t = consume_tile(cur, tslot, tph, fed, true)) {
       const typename P::Tile tile = P::tile(p, *sched, t);
       bool ok = mbar_wait(&tfull[buf], bph, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
@@ -389,6 +472,16 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (DYN) {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.sched_counters + 1, 1u) == gridDim.x - 1) {
+        p.sched_counters[0] = 0;  // every CTA has taken its last tile
+        p.sched_counters[1] = 0;
+        __threadfence();
+      }
+    }
+  }
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
