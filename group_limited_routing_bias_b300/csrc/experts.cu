@@ -50,6 +50,12 @@ struct ExpertGemm {
   static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static constexpr bool DYNAMIC = true;  // tiles taken from a global counter
+  // The down GEMM is launched as a programmatic dependent of gate/up: its CTAs
+  // start on SMs that gate/up no longer needs, and each down tile waits only
+  // for its own expert's h rows (counted per expert as the gate/up epilogue
+  // warps store them), so the gate/up tail and the launch gap overlap work.
+  static constexpr bool PDL_PRIMARY = GATEUP;
+  static constexpr bool PDL_SECONDARY = !GATEUP;
 
   struct Params {
     CUtensorMap tmap_a0;  // weights [E * a_rows, K]: W_gate or W_down
@@ -66,10 +72,12 @@ struct ExpertGemm {
     const uint8_t *wp0, *wp1;
     int ktiles;  // 64-wide k blocks per weight row
     uint32_t *sched_counters;  // dynamic tile schedule (workspace header)
+    uint32_t *expert_done;     // [E] gate/up epilogue warps done per expert (workspace header)
+    int up_mt;                 // gate/up feature tiles per token tile (down: readiness target)
   };
   using Sched = ExpertSched;
   struct Tile {
-    int row0, nrows, arow0, m;
+    int row0, nrows, arow0, m, e, ntt;  // ntt: token tiles of expert e
   };
   static constexpr bool CONVERT = false;
   static constexpr bool F16 = false;
@@ -114,7 +122,45 @@ struct ExpertGemm {
     const int e = lo;
     const int row0 = s.off[e] + (tti - s.tt[e]) * BN;
     const int nrows = min(BN, s.off[e + 1] - row0);
-    return Tile{row0, nrows, e * p.a_rows + m * kTileM, m};
+    return Tile{row0, nrows, e * p.a_rows + m * kTileM, m, e, s.tt[e + 1] - s.tt[e]};
+  }
+  // gate/up: each epilogue warp publishes its 32 features of h for the tile
+  // (release: its stores before the count, for the down GEMM's TMA reads)
+  __device__ static void tile_done(const Params &p, const Tile &t) {
+    if constexpr (GATEUP) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __threadfence();
+      atomicAdd(p.expert_done + t.e, 1u);
+    }
+  }
+  // down: wait until every gate/up tile of the expert (4 epilogue warps each)
+  // has been published, then order the TMA reads of h after that
+  __device__ static bool tile_ready(const Params &p, const Tile &t, volatile int *abort) {
+    if constexpr (GATEUP) {
+      return true;
+    } else {
+      const uint32_t need = 4u * (uint32_t)p.up_mt * (uint32_t)t.ntt;
+      const uint32_t *cnt = p.expert_done + t.e;
+      if (ld_acquire_gpu(cnt) < need) {
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_gpu(cnt) < need) {
+          if (*abort) return false;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicOr(p.status, (uint32_t)MOE_DEV_TIMEOUT);
+            return false;
+          }
+          __nanosleep(100);
+        }
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+  }
+  // down, last CTA: every count has been consumed; zero them for the next call
+  __device__ static void last_cta(const Params &p) {
+    if constexpr (!GATEUP)
+      for (int e = 0; e < p.E; ++e) p.expert_done[e] = 0;
   }
   __device__ static int num_k(const Params &p, const Tile &) { return p.ksteps; }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
@@ -335,7 +381,24 @@ moe_status launch_gemm(const typename P::Params &prm, int grid, cudaStream_t str
       return MOE_ERR_CUDA;
     attr_set = true;
   }
-  tc_gemm_kernel<P><<<grid, 256, smem, stream>>>(prm);
+  if constexpr (PdlSecondaryOf<P>::value) {
+    // A programmatic dependent of the previous launch.  Its CTAs never share an
+    // SM with the primary's (each needs more than half the shared memory).
+    static_assert(smem > kSmemLimit / 2, "dependent launch must not share SMs with its primary");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel<P>, prm) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    tc_gemm_kernel<P><<<grid, 256, smem, stream>>>(prm);
+  }
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -365,6 +428,8 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     prm.mt = d.I / kTileM;
     prm.status = status;
     prm.sched_counters = status + kSchedCounterWord;
+    prm.expert_done = status + kExpertDoneWord;
+    prm.up_mt = prm.mt;
     const bool tiled = ex.layout == MOE_LAYOUT_TILED;
     prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_gate) : nullptr;
     prm.wp1 = tiled ? static_cast<const uint8_t *>(ex.w_up) : nullptr;
@@ -390,7 +455,9 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     prm.ksteps = d.I / (kTileK * P::KSUB);
     prm.mt = d.H / kTileM;
     prm.status = status;
-    prm.sched_counters = status + kSchedCounterWord;
+    prm.sched_counters = status + kSchedCounterWord + 2;  // runs alongside gate/up's
+    prm.expert_done = status + kExpertDoneWord;
+    prm.up_mt = d.I / kTileM;
     const bool tiled = ex.layout == MOE_LAYOUT_TILED;
     prm.wp0 = tiled ? static_cast<const uint8_t *>(ex.w_down) : nullptr;
     prm.wp1 = nullptr;

@@ -15,11 +15,13 @@ namespace beam {
 
 constexpr int kTargetCtas = 148;       // B300 SM count; sizes the router's K split
 constexpr int kPermuteChunk = 4096;    // entries per permute CTA (32 warps x 128)
-constexpr size_t kHeaderBytes = 256;   // workspace status header
-// Header layout (uint32 words): [0] the device status word; [32], [33] the
-// counters of the dynamic tile schedule (next tile, finished CTAs), zero
-// between launches.
+constexpr size_t kHeaderBytes = 2048;  // workspace status header
+// Header layout (uint32 words): [0] the device status word; [32..35] the
+// counters of the dynamic tile schedule (next tile, finished CTAs) of the
+// gate/up and the down GEMM; [64, 64 + E) per-expert counts of published
+// gate/up tiles.  All zero between calls.
 constexpr size_t kSchedCounterWord = 32;
+constexpr size_t kExpertDoneWord = 64;
 constexpr int kMaxRouterSplit = 20;    // router K split; the top-k kernel adds the partials
 
 inline int ilog2(int v) {

@@ -47,6 +47,10 @@ void *scratch_address(moe_status *st) {
 
 using namespace beam;
 
+namespace {
+constexpr size_t kNoAllocHeaderBytes = 256;  // status word, then the tables
+}
+
 extern "C" moe_status moe_permute_noalloc(const moe_dims *dims, const int32_t *topk_idx,
                                           const void *x, void *x_perm, int32_t *expert_offsets,
                                           int32_t *slot_of, int32_t *row_src,
@@ -61,14 +65,14 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims *dims, const int32_t *t
   const size_t Tk = (size_t)dims->T * dims->top_k;
   const size_t nchunks = std::max<size_t>(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
   const size_t table = ((nchunks * dims->E * sizeof(int32_t)) + 255) & ~(size_t)255;
-  if (kHeaderBytes + 2 * table > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+  if (kNoAllocHeaderBytes + 2 * table > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
   char *base = static_cast<char *>(scratch_address(&st));
   if (st != MOE_OK) return st;
   // Every word of the counts and bases tables is written before it is read
   // within one call, so nothing is cleared between calls.
   uint32_t *status = reinterpret_cast<uint32_t *>(base);
-  int32_t *counts = reinterpret_cast<int32_t *>(base + kHeaderBytes);
-  int32_t *bases = reinterpret_cast<int32_t *>(base + kHeaderBytes + table);
+  int32_t *counts = reinterpret_cast<int32_t *>(base + kNoAllocHeaderBytes);
+  int32_t *bases = reinterpret_cast<int32_t *>(base + kNoAllocHeaderBytes + table);
   return launch_permute(*dims, topk_idx, x, x_perm, expert_offsets, slot_of, row_src, counts, bases,
                         status, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -34,6 +34,21 @@
 // (sched_counters[1] counts finished CTAs), so they start at zero for the next
 // launch; they must be zero before the first.
 //
+// Optional hooks for a producer/consumer pair of launches (the decode gate/up
+// and down GEMMs), all default off:
+//   static constexpr bool PDL_PRIMARY;    every CTA allows the next launch (a
+//                                         programmatic dependent) to start once
+//                                         SMs free up (griddepcontrol.launch_dependents)
+//   static constexpr bool PDL_SECONDARY;  launched as that dependent: the CTAs wait
+//                                         for the primary grid only before exiting
+//   static bool tile_ready(const Params&, const Tile&, volatile int *abort)
+//                                         producer, before a tile's first load
+//                                         (false: gave up, the CTA aborts)
+//   static void tile_done(const Params&, const Tile&)
+//                                         lane 0 of each of the four epilogue warps,
+//                                         after the warp stored its rows of the tile
+//   static void last_cta(const Params&)   the last CTA to finish (dynamic schedule)
+//
 // A problem class P supplies the shapes and the tile schedule:
 //   static constexpr int BN, NA, STAGES, NBUF, TX_BYTES (or a tx_bytes hook, below);
 //   static constexpr bool CONVERT, F16;   (packed weights; f16 instead of bf16 operands)
@@ -135,6 +150,41 @@ struct DynamicOf<P, std::void_t<decltype(P::DYNAMIC)>> {
 };
 
 constexpr int kTileRing = 4;
+
+template <class P, class = void>
+struct PdlPrimaryOf {
+  static constexpr bool value = false;
+};
+template <class P>
+struct PdlPrimaryOf<P, std::void_t<decltype(P::PDL_PRIMARY)>> {
+  static constexpr bool value = P::PDL_PRIMARY;
+};
+template <class P, class = void>
+struct PdlSecondaryOf {
+  static constexpr bool value = false;
+};
+template <class P>
+struct PdlSecondaryOf<P, std::void_t<decltype(P::PDL_SECONDARY)>> {
+  static constexpr bool value = P::PDL_SECONDARY;
+};
+template <class P, class = void>
+struct HasTileReady : std::false_type {};
+template <class P>
+struct HasTileReady<P, std::void_t<decltype(P::tile_ready(std::declval<const typename P::Params &>(),
+                                                           std::declval<const typename P::Tile &>(),
+                                                           std::declval<volatile int *>()))>>
+    : std::true_type {};
+template <class P, class = void>
+struct HasTileDone : std::false_type {};
+template <class P>
+struct HasTileDone<P, std::void_t<decltype(P::tile_done(std::declval<const typename P::Params &>(),
+                                                         std::declval<const typename P::Tile &>()))>>
+    : std::true_type {};
+template <class P, class = void>
+struct HasLastCta : std::false_type {};
+template <class P>
+struct HasLastCta<P, std::void_t<decltype(P::last_cta(std::declval<const typename P::Params &>()))>>
+    : std::true_type {};
 
 template <class P>
 __host__ __device__ constexpr int threads_for() {
@@ -248,6 +298,7 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int ntiles = P::num_tiles(p, *sched);
+  if constexpr (PdlPrimaryOf<P>::value) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Tile feed.  `cur` is the static cursor; slot / tph index the tile ring.
   // The producer publishes each tile it takes (-1 at the end); consumers read
@@ -310,6 +361,12 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
            t = produce_tile(cur, tslot, tph, ok)) {
         const typename P::Tile tile = P::tile(p, *sched, t);
         const int nk = P::num_k(p, tile);
+        if constexpr (HasTileReady<P>::value) {
+          if (!P::tile_ready(p, tile, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
         for (int k = 0; k < nk; ++k) {
           if constexpr (P::CONVERT) {
             if (raw_role) {
@@ -463,6 +520,9 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
+      if constexpr (HasTileDone<P>::value) {
+        if (lane == 0) P::tile_done(p, tile);
+      }
       if (++buf == P::NBUF) {
         buf = 0;
         bph ^= 1u;
@@ -478,6 +538,7 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       if (atomicAdd(p.sched_counters + 1, 1u) == gridDim.x - 1) {
         p.sched_counters[0] = 0;  // every CTA has taken its last tile
         p.sched_counters[1] = 0;
+        if constexpr (HasLastCta<P>::value) P::last_cta(p);
         __threadfence();
       }
     }
@@ -486,6 +547,8 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // A dependent launch: order this grid's completion after the primary's.
+  if constexpr (PdlSecondaryOf<P>::value) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace beam

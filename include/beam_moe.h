@@ -23,7 +23,11 @@
  *     status word at the start of the workspace; read it with
  *     moe_workspace_status after the stream has finished.
  *   - Workspaces must be at least moe_workspace_size(...) bytes and their
- *     first 256 bytes zeroed once before first use (moe_workspace_init).
+ *     first 2048 bytes zeroed once before first use (moe_workspace_init);
+ *     calls leave them zeroed again (they hold the status word and the
+ *     counters of the expert GEMMs' tile schedule).  After a call that
+ *     returned an error or set a device status bit, zero them again
+ *     (moe_workspace_init) before reusing the workspace.
  *     A workspace may be reused by consecutive calls on one stream; calls
  *     that run concurrently need separate workspaces.
  *   - Shape limits: H % 128 == 0, I % 128 == 0, E <= 256 with E % 32 == 0,
@@ -148,10 +152,10 @@ const char *moe_status_string(moe_status s);
 moe_status moe_check_dims(const moe_dims *dims);
 
 /* Bytes of workspace that entry point `op` needs for these dims (0 if the
- * dims are unsupported).  Includes the 256-byte status header. */
+ * dims are unsupported).  Includes the 2048-byte status header. */
 size_t moe_workspace_size(const moe_dims *dims, moe_wdtype wdtype, moe_op op);
 
-/* Zeroes the 256-byte status header of a workspace (asynchronous). */
+/* Zeroes the 2048-byte status header of a workspace (asynchronous). */
 moe_status moe_workspace_init(void *ws, moe_stream_t stream);
 
 /* Synchronises `stream`, then copies the workspace status word into

@@ -1,7 +1,9 @@
-"""Dynamic tile schedule of the weights-on-M bf16 expert GEMMs: tiles are taken
-from two counters in the workspace header, which every launch must leave at
-zero.  Repeated calls (and a CUDA graph replayed several times) give
-bit-identical results, and the counters read back as zero after each."""
+"""Dynamic tile schedule and per-expert readiness counts of the weights-on-M
+bf16 expert GEMMs (the down GEMM runs as a programmatic dependent of gate/up
+and waits per expert for its h rows): the counters live in the workspace
+header and every call must leave them at zero.  Repeated calls (and a CUDA
+graph replayed several times) give bit-identical results, and the counters
+read back as zero after each."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +12,8 @@ import moe_inputs as mi
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-SCHED_WORDS = slice(32, 34)  # header words of the schedule counters
+SCHED_WORDS = slice(32, 36)  # header words of the two schedule counter pairs
+DONE_WORDS = slice(64, 64 + 256)  # per-expert published gate/up tiles
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +24,7 @@ def lib():
 
 def header_words(ws):
     torch.cuda.synchronize()
-    return ws[:256].view(torch.int32).cpu().numpy()
+    return ws[:2048].view(torch.int32).cpu().numpy()
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 64), ("decode", 64)])
@@ -36,7 +39,7 @@ def test_repeated_forwards_identical_and_counters_zero(lib, name, T):
         y = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=DEV)
         lib.moe_forward(d, x, wr, b, ex, y, ws)
         h = header_words(ws)
-        assert h[0] == 0 and not h[SCHED_WORDS].any(), h[:40]
+        assert h[0] == 0 and not h[SCHED_WORDS].any() and not h[DONE_WORDS].any(), h[:80]
         ys.append(y)
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
@@ -64,5 +67,5 @@ def test_graph_replays_identical_and_counters_zero(lib):
         y.zero_()
         g.replay()
         h = header_words(ws)
-        assert h[0] == 0 and not h[SCHED_WORDS].any(), h[:40]
+        assert h[0] == 0 and not h[SCHED_WORDS].any() and not h[DONE_WORDS].any(), h[:80]
         assert torch.equal(y, ref)
