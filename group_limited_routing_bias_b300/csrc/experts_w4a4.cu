@@ -440,20 +440,25 @@ __global__ void __launch_bounds__(256)
 
 // The dispatch's form for the forward pass: token t is quantised once and its
 // codes and scales are written to every permuted row that holds one of its
-// entries (slot_of[t*k + j]; dropped entries have slot -1).  One warp per token.
+// entries (slot_of[t*k + j]; dropped entries have slot -1).  One warp per
+// (token, 32 blocks of its row), one 16-value block per lane, so a small batch
+// still spreads over many warps.
 __global__ void __launch_bounds__(256)
     quantize_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
                             int T, int top_k, int cols, float g, uint2 *__restrict__ q,
                             uint8_t *__restrict__ s) {
   const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
   const int nblk = cols / 16;
+  const int segs = (nblk + 31) / 32;
   const float six_g = 6.0f * g;
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+  for (long w = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < (long)T * segs;
+       w += nwarps) {
+    const int t = (int)(w / segs);
     const uint4 *xr = x + (size_t)t * (cols / 8);
     const int my_slot = lane < top_k ? __ldg(slot_of + (size_t)t * top_k + lane) : -1;
-    for (int b0 = 0; b0 < nblk; b0 += 32) {  // whole warp each step: the slots are shuffled
-      const int b = b0 + lane;
+    {  // whole warp: the slots are shuffled
+      const int b = (int)(w - (long)t * segs) * 32 + lane;
       uint2 codes = make_uint2(0u, 0u);
       uint8_t sc = 0;
       if (b < nblk) {
@@ -485,7 +490,8 @@ moe_status launch_quantize_scatter_nvfp4(const void *x, const int32_t *slot_of, 
                                          int cols, float g, uint8_t *q, uint8_t *s,
                                          cudaStream_t stream) {
   if (T <= 0) return MOE_OK;
-  const int blocks = std::max(1, std::min((T + 7) / 8, device_sm_count() * 8));
+  const long tasks = (long)T * ((cols / 16 + 31) / 32);
+  const int blocks = (int)std::max<long>(1, std::min<long>((tasks + 7) / 8, device_sm_count() * 8));
   quantize_scatter_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4 *>(x), slot_of, T,
                                                      top_k, cols, g, reinterpret_cast<uint2 *>(q),
                                                      s);

@@ -22,7 +22,7 @@ constexpr size_t kHeaderBytes = 2048;  // workspace status header
 // gate/up tiles.  All zero between calls.
 constexpr size_t kSchedCounterWord = 32;
 constexpr size_t kExpertDoneWord = 64;
-constexpr int kMaxRouterSplit = 20;    // router K split; the top-k kernel adds the partials
+constexpr int kMaxRouterSplit = 60;    // router K split; the top-k kernel adds the partials
 
 inline int ilog2(int v) {
   int r = 0;

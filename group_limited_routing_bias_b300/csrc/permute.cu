@@ -8,7 +8,8 @@
 //   permute_count_kernel   one CTA per chunk of 4096 entries: histogram
 //   permute_scan_kernel    one CTA: per-chunk bases and expert offsets
 //   permute_scatter_kernel one CTA per chunk: warp-ordered ranks -> slots
-//   permute_scatter_rows_kernel  all SMs: each token's x row to its k slots (16-byte vectors)
+//   permute_scatter_rows_kernel  all SMs: each token's x row to its k slots (16-byte
+//                          vectors, one warp per 2 KB segment of a row)
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
@@ -202,35 +203,47 @@ __global__ void __launch_bounds__(kChunkThreads)
 // when x is larger than L2 (prefill: an expert-ordered gather would fetch each
 // row from DRAM up to k times).  With TO_F16 the bf16 values are written as
 // f16 (exact for |v| >= 2^-14; the packed-weight GEMMs run on f16 operands).
-// One warp per token, one 16-byte vector per lane and step.
+// One warp per (token, 128-vector segment of its row): each lane loads its
+// four 16-byte vectors of the segment first, then stores them to the token's
+// k slots, so a warp has all its loads in flight at once and a small batch
+// still spreads over many warps.
+constexpr int kScatterSeg = 128;  // 16-byte vectors per warp task (4 per lane)
+
 template <bool TO_F16>
 __global__ void __launch_bounds__(256)
     permute_scatter_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
                                 int T, int top_k, int vec_per_row, uint4 *__restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+  const int segs = (vec_per_row + kScatterSeg - 1) / kScatterSeg;
+  const long ntasks = (long)T * segs;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  for (long w = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < ntasks; w += nwarps) {
+    const int t = (int)(w / segs);
+    const int v0 = (int)(w - (long)t * segs) * kScatterSeg + lane;
     const int my_slot = lane < top_k ? __ldg(slot_of + (size_t)t * top_k + lane) : -1;
     const uint4 *src = x + (size_t)t * vec_per_row;
-    for (int v0 = 0; v0 < vec_per_row; v0 += 32) {  // whole warp each step: slots are shuffled
-      const int v = v0 + lane;
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      if (v < vec_per_row) {
-        q = src[v];
-        if (TO_F16) {
-          uint32_t *w = reinterpret_cast<uint32_t *>(&q);
+    uint4 q[kScatterSeg / 32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-            const __half2 h = __float22half2_rn(f);
-            w[i] = *reinterpret_cast<const uint32_t *>(&h);
-          }
+    for (int i = 0; i < kScatterSeg / 32; ++i) {
+      const int v = v0 + 32 * i;
+      q[i] = v < vec_per_row ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+      if (TO_F16) {
+        uint32_t *wd = reinterpret_cast<uint32_t *>(&q[i]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wd[c]));
+          const __half2 h = __float22half2_rn(f);
+          wd[c] = *reinterpret_cast<const uint32_t *>(&h);
         }
       }
-      for (int j = 0; j < top_k; ++j) {
-        const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-        if (slot >= 0 && v < vec_per_row) x_perm[(size_t)slot * vec_per_row + v] = q;
-      }
+    }
+    for (int j = 0; j < top_k; ++j) {
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);  // the same in every lane
+      if (slot < 0) continue;
+      uint4 *dst = x_perm + (size_t)slot * vec_per_row;
+#pragma unroll
+      for (int i = 0; i < kScatterSeg / 32; ++i)
+        if (v0 + 32 * i < vec_per_row) dst[v0 + 32 * i] = q[i];
     }
   }
 }
@@ -263,7 +276,8 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
         topk_idx, Tk, d.E, bases, slot_of, row_src);
   }
   if (Tk > 0 && gather != kGatherNone) {
-    const int blocks = std::max(1, std::min((d.T + 7) / 8, device_sm_count() * 8));
+    const long tasks = (long)d.T * ((d.H / 8 + kScatterSeg - 1) / kScatterSeg);
+    const int blocks = (int)std::max<long>(1, std::min<long>((tasks + 7) / 8, device_sm_count() * 8));
     if (gather == kGatherF16)
       permute_scatter_rows_kernel<true><<<blocks, 256, 0, stream>>>(
           static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8,
