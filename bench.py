@@ -257,14 +257,16 @@ def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
     return out
 
 
-def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks, a4=None, tiled=False):
-    """Packed experts (NVFP4 or FP8): decode T=64 (HBM-bound: packed bytes of
-    touched experts) and prefill T=16384 (W4A16 / W8A16: the bf16 tensor peak
-    is its denominator; W4A4 (a4 given): the fp4 peak, the measured bf16 peak
-    times the nominal fp4/bf16 ratio 13.5/2.25).  tiled: the weights in the
-    tiled layout of moe_pack_nvfp4 / moe_pack_fp8."""
+def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks, a4=None, tiled=False,
+                   extra_T=()):
+    """Packed experts (NVFP4 or FP8): decode T=64, and each T in extra_T (HBM-bound:
+    packed bytes of touched experts), and prefill T=16384 (W4A16 / W8A16: the bf16
+    tensor peak is its denominator; W4A4 (a4 given): the fp4 peak, the measured
+    bf16 peak times the nominal fp4/bf16 ratio 13.5/2.25).  tiled: the weights in
+    the tiled layout of moe_pack_nvfp4 / moe_pack_fp8."""
     out = {"layout": "tiled" if tiled else "row-major"}
-    for name, T, steps in (("decode", 64, 50), ("prefill", 16384, 5)):
+    runs = [("decode", 64, 50)] + [(f"T{t}", t, 20) for t in extra_T] + [("prefill", 16384, 5)]
+    for name, T, steps in runs:
         cfg = mi.CONFIGS[fmt].with_T(T)
         wl = Workload(lib, cfg, wts, dev, a4=a4, tiled=tiled)
         for _ in range(3):
@@ -276,7 +278,7 @@ def packed_figures(lib, mi, fmt, wts, expert_bytes, dev, flush, peaks, a4=None, 
         touched = int(len(np.unique(wl.idx.cpu().numpy())))
         fig = {"T": T, "tokens_per_s": T / (ms / 1000.0), "ms_per_step": ms, "stages_ms": st,
                "touched_experts": touched}
-        if name == "decode":
+        if name != "prefill":
             gbs = touched * expert_bytes / (st["experts"] / 1000.0) / 1e9
             fig.update({"expert_gemm_gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm"],
                         "frac_of_8tbs_nominal": gbs / 8000.0})
@@ -568,9 +570,9 @@ def main():
         packed = [mi.quantize_experts_nvfp4(w) for w in weights]
         fp4w = tuple(p[0] for p in packed) + tuple(p[1] for p in packed) + tuple(p[2] for p in packed)
         nvfp4 = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks,
-                               tiled=True)
+                               tiled=True, extra_T=(1, 1024))
         nvfp4["w4a4"] = packed_figures(lib, mi, "nvfp4", fp4w, FP4_EXPERT_BYTES, dev, flush, peaks,
-                                       a4=(mi.A4_X_GLOBAL, mi.A4_H_GLOBAL))
+                                       a4=(mi.A4_X_GLOBAL, mi.A4_H_GLOBAL), extra_T=(1, 1024))
         del packed, fp4w
         torch.cuda.empty_cache()
         packed = [mi.quantize_experts_fp8(w) for w in weights]
