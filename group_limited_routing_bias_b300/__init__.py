@@ -27,7 +27,8 @@ MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0x1, 0x2
 MOE_LAYOUT_ROWMAJOR, MOE_LAYOUT_TILED = 0, 1
 
 EXPORTED = ("moe_version", "moe_status_string", "moe_check_dims", "moe_workspace_size",
-            "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_permute",
+            "moe_workspace_init", "moe_workspace_status", "moe_route", "moe_route_logits",
+            "moe_permute",
             "moe_experts_swiglu", "moe_combine", "moe_forward", "moe_bias_update",
             "moe_quantize_nvfp4", "moe_pack_bf16", "moe_pack_nvfp4", "moe_pack_fp8",
             "moe_permute_noalloc")
@@ -58,6 +59,7 @@ _sig = {
     "moe_workspace_init": ([_P, _P], _I),
     "moe_workspace_status": ([_P, _P, ctypes.POINTER(ctypes.c_uint32)], _I),
     "moe_route": ([_DP, _P, _P, _P, _P, _P, _P, _S, _P], _I),
+    "moe_route_logits": ([_DP, _P, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "moe_permute": ([_DP, _P, _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "moe_experts_swiglu": ([_DP, ctypes.POINTER(MoeExperts), _P, _P, _P, _P, _P, _P, _S, _P], _I),
     "moe_combine": ([_DP, _P, _P, _P, _P], _I),
@@ -267,6 +269,17 @@ def moe_route(d: MoeDims, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
         ctypes.byref(d), _ptr(x, torch.bfloat16, (T, H), "x"),
         _ptr(w_router, torch.float32, (E, H), "w_router"), _ptr(bias, torch.float32, (E,), "bias"),
         _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
+        _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
+
+
+def moe_route_logits(d: MoeDims, x, w_router, bias, topk_idx, topk_w, logits, ws, stream=None):
+    """Router as moe_route, plus the fp32 logits [T, E] the selection was made from."""
+    T, H, E, k = d.T, d.H, d.E, d.top_k
+    _check("moe_route_logits", native().moe_route_logits(
+        ctypes.byref(d), _ptr(x, torch.bfloat16, (T, H), "x"),
+        _ptr(w_router, torch.float32, (E, H), "w_router"), _ptr(bias, torch.float32, (E,), "bias"),
+        _ptr(topk_idx, torch.int32, (T, k), "topk_idx"), _ptr(topk_w, torch.float32, (T, k), "topk_w"),
+        _ptr(logits, torch.float32, (T, E), "logits"),
         _ptr(ws, torch.uint8, name="ws"), ws.numel(), _stream(stream)))
 
 

@@ -3,6 +3,8 @@
 // entry point.  Every check happens before the first launch; nothing here
 // allocates device memory or synchronises (except moe_workspace_status).
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "moe_internal.cuh"
 
@@ -69,6 +71,20 @@ int device_sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+moe_status ensure_smem_limit(const void *kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void *, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return MOE_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  done.insert({kernel, dev});
+  return MOE_OK;
 }
 
 }  // namespace beam
@@ -203,6 +219,20 @@ moe_status moe_route(const moe_dims *dims, const void *x, const float *w_router,
   return launch_route(*dims, x, w_router, bias, topk_idx, topk_w, make_router_plan(*dims),
                       at<__nv_bfloat16>(ws, L.w3), at<float>(ws, L.partial), status_word(ws),
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route_logits(const moe_dims *dims, const void *x, const float *w_router,
+                            const float *bias, int32_t *topk_idx, float *topk_w, float *logits,
+                            void *ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (dims->T == 0) return MOE_OK;
+  if (!ptrs_ok({x, w_router, bias, topk_idx, topk_w, logits})) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(dims, MOE_OP_ROUTE, ws, ws_bytes)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*dims, MOE_OP_ROUTE);
+  return launch_route(*dims, x, w_router, bias, topk_idx, topk_w, make_router_plan(*dims),
+                      at<__nv_bfloat16>(ws, L.w3), at<float>(ws, L.partial), status_word(ws),
+                      reinterpret_cast<cudaStream_t>(stream), logits);
 }
 
 moe_status moe_permute(const moe_dims *dims, const int32_t *topk_idx, const void *x, void *x_perm,

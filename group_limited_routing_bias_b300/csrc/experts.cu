@@ -14,6 +14,7 @@
 // so silu(g) * u is formed in the epilogue without another pass; the down
 // projection scales each token row by its routing weight in its epilogue.
 #include "moe_internal.cuh"
+#include "sched.cuh"
 #include "tc_gemm.cuh"
 
 namespace beam {
@@ -26,15 +27,6 @@ template <>
 __device__ __forceinline__ void tmem_ld_chunk<32>(uint32_t taddr, uint32_t (&r)[32]) {
   tmem_ld32(taddr, r);
 }
-template <>
-__device__ __forceinline__ void tmem_ld_chunk<16>(uint32_t taddr, uint32_t (&r)[16]) {
-  tmem_ld16(taddr, r);
-}
-
-struct ExpertSched {
-  int off[257];  // expert row offsets
-  int tt[257];   // prefix of token tiles per expert
-};
 
 template <int BN_, bool GATEUP>
 struct ExpertGemm {
@@ -46,7 +38,7 @@ struct ExpertGemm {
   static constexpr int KSUB = BN <= 64 ? 2 : 1;
   static constexpr int STAGE_BYTES = StageGeom<BN, NA>::kBytes * KSUB;
   static constexpr int STAGES_FIT =
-      (kSmemLimit - kSmemReserve - (int)sizeof(ExpertSched)) / STAGE_BYTES;
+      (kSmemLimit - kSmemReserve - (int)sizeof(TileSched)) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static constexpr bool DYNAMIC = true;  // tiles taken from a global counter
@@ -60,7 +52,8 @@ struct ExpertGemm {
   struct Params {
     CUtensorMap tmap_a0;  // weights [E * a_rows, K]: W_gate or W_down
     CUtensorMap tmap_a1;  // W_up (gate/up only)
-    CUtensorMap tmap_b;   // token rows [Tk, K]: x_perm or h
+    CUtensorMap tmap_b;   // token rows [Tk, K]: x_perm or h, box of BN rows
+    CUtensorMap tmap_bh;  // the same rows, box of BN / 2 rows
     const int32_t *offsets;
     const int32_t *row_src;
     const float *topk_w;
@@ -75,7 +68,7 @@ struct ExpertGemm {
     uint32_t *expert_done;     // [E] gate/up epilogue warps done per expert (workspace header)
     int up_mt;                 // gate/up feature tiles per token tile (down: readiness target)
   };
-  using Sched = ExpertSched;
+  using Sched = TileSched;
   struct Tile {
     int row0, nrows, arow0, m, e, ntt;  // ntt: token tiles of expert e
   };
@@ -83,46 +76,27 @@ struct ExpertGemm {
   static constexpr bool F16 = false;
   static constexpr int RAW_BYTES = 0;
   static constexpr int RSTAGES = 0;
-  static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes * KSUB;
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 
-  __device__ static void prologue(const Params &p, Sched &s) {
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.off[i] = p.offsets[i];
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      const int per = (p.E + 31) / 32;
-      const int e0 = lane * per;
-      int local = 0;
-      for (int e = e0; e < e0 + per && e < p.E; ++e) local += (s.off[e + 1] - s.off[e] + BN - 1) / BN;
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int run = incl - local;
-      for (int e = e0; e < e0 + per && e < p.E; ++e) {
-        s.tt[e] = run;
-        run += (s.off[e + 1] - s.off[e] + BN - 1) / BN;
-      }
-      if (lane == 31) s.tt[p.E] = incl;
-    }
-    __syncthreads();
+  // Token rows a tile loads: a tile of at most BN / 2 rows loads the half box
+  // (the MMA still reads BN rows; the columns of rows past the tile's own are
+  // never stored), so an expert of up to BN rows streams its weights once at
+  // the cost of a BN / 2 box.
+  __device__ static int box_rows(const Tile &t) { return t.nrows <= BN / 2 ? BN / 2 : BN; }
+  __device__ static uint32_t tx_bytes(const Params &, const Tile &t) {
+    return (uint32_t)KSUB * (NA * kATileBytes + box_rows(t) * kTileK * 2);
   }
-  __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tt[p.E] * p.mt; }
+
+  __device__ static void prologue(const Params &p, Sched &s) {
+    tile_sched_prologue(p.offsets, p.E, BN, 1, s);
+  }
+  __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E] * p.mt; }
   __device__ static Tile tile(const Params &p, const Sched &s, int t) {
     const int tti = t / p.mt, m = t - tti * p.mt;
-    int lo = 0, hi = p.E;  // last e with tt[e] <= tti
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s.tt[mid] <= tti) lo = mid;
-      else hi = mid;
-    }
-    const int e = lo;
-    const int row0 = s.off[e] + (tti - s.tt[e]) * BN;
+    const int e = tile_sched_expert(s, p.E, tti);
+    const int row0 = s.off[e] + (tti - s.tp[e]) * BN;
     const int nrows = min(BN, s.off[e + 1] - row0);
-    return Tile{row0, nrows, e * p.a_rows + m * kTileM, m, e, s.tt[e + 1] - s.tt[e]};
+    return Tile{row0, nrows, e * p.a_rows + m * kTileM, m, e, s.tp[e + 1] - s.tp[e]};
   }
   // gate/up: each epilogue warp publishes its 32 features of h for the tile
   // (release: its stores before the count, for the down GEMM's TMA reads)
@@ -176,7 +150,8 @@ struct ExpertGemm {
         tma_load_2d(st, &p.tmap_a0, bar, kb * kTileK, t.arow0);
         if (GATEUP) tma_load_2d(st + kATileBytes, &p.tmap_a1, bar, kb * kTileK, t.arow0);
       }
-      tma_load_2d(st + NA * kATileBytes, &p.tmap_b, bar, kb * kTileK, t.row0);
+      tma_load_2d(st + NA * kATileBytes, box_rows(t) == BN ? &p.tmap_b : &p.tmap_bh, bar,
+                  kb * kTileK, t.row0);
     }
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
@@ -218,11 +193,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-struct TokenMajorSched {
-  int off[257];  // expert row offsets
-  int tp[257];   // prefix of tiles per expert (token tiles x feature tiles)
-};
-
 // Token-major expert GEMM for larger batches: 128 token rows of one expert on
 // the MMA's M side, 256 weight rows on the N side.  Gate/up: the N side is the
 // 128 gate rows and the 128 up rows of the same 128 features, so each thread
@@ -254,7 +224,7 @@ struct ExpertGemmTM {
     const uint8_t *wp0, *wp1;  // MMA-tiled weights (moe_pack_bf16), or null
     int ktiles;                // 64-wide k blocks per weight row
   };
-  using Sched = TokenMajorSched;
+  using Sched = TileSched;
   struct Tile {
     int row0, nrows, brow0, f;
   };
@@ -265,39 +235,11 @@ struct ExpertGemmTM {
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
 
   __device__ static void prologue(const Params &p, Sched &s) {
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.off[i] = p.offsets[i];
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      const int per = (p.E + 31) / 32;
-      const int e0 = lane * per;
-      int local = 0;
-      for (int e = e0; e < e0 + per && e < p.E; ++e)
-        local += (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM * p.nf;
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int run = incl - local;
-      for (int e = e0; e < e0 + per && e < p.E; ++e) {
-        s.tp[e] = run;
-        run += (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM * p.nf;
-      }
-      if (lane == 31) s.tp[p.E] = incl;
-    }
-    __syncthreads();
+    tile_sched_prologue(p.offsets, p.E, kTileM, p.nf, s);
   }
   __device__ static int num_tiles(const Params &p, const Sched &s) { return s.tp[p.E]; }
   __device__ static Tile tile(const Params &p, const Sched &s, int t) {
-    int lo = 0, hi = p.E;  // last e with tp[e] <= t
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s.tp[mid] <= t) lo = mid;
-      else hi = mid;
-    }
-    const int e = lo;
+    const int e = tile_sched_expert(s, p.E, t);
     const int ntt = (s.off[e + 1] - s.off[e] + kTileM - 1) / kTileM;
     const int local = t - s.tp[e];
     const int f = local / ntt, tt = local - f * ntt;
@@ -374,13 +316,7 @@ struct ExpertGemmTM {
 template <class P>
 moe_status launch_gemm(const typename P::Params &prm, int grid, cudaStream_t stream) {
   constexpr int smem = smem_bytes_for<P>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_smem_limit((const void *)tc_gemm_kernel<P>, smem) != MOE_OK) return MOE_ERR_CUDA;
   if constexpr (PdlSecondaryOf<P>::value) {
     // A programmatic dependent of the previous launch.  Its CTAs never share an
     // SM with the primary's (each needs more than half the shared memory).
@@ -415,7 +351,8 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     typename P::Params prm;
     if (!make_tmap_bf16_2d(&prm.tmap_a0, ex.w_gate, d.H, (uint64_t)d.E * d.I, kTileM) ||
         !make_tmap_bf16_2d(&prm.tmap_a1, ex.w_up, d.H, (uint64_t)d.E * d.I, kTileM) ||
-        !make_tmap_bf16_2d(&prm.tmap_b, x_perm, d.H, Tk, BN))
+        !make_tmap_bf16_2d(&prm.tmap_b, x_perm, d.H, Tk, BN) ||
+        !make_tmap_bf16_2d(&prm.tmap_bh, x_perm, d.H, Tk, BN / 2))
       return MOE_ERR_CUDA;
     prm.offsets = offsets;
     prm.row_src = row_src;
@@ -442,7 +379,8 @@ moe_status launch_experts_bn(const moe_dims &d, const moe_experts &ex, const voi
     using P = ExpertGemm<BN, false>;
     typename P::Params prm;
     if (!make_tmap_bf16_2d(&prm.tmap_a0, ex.w_down, d.I, (uint64_t)d.E * d.H, kTileM) ||
-        !make_tmap_bf16_2d(&prm.tmap_b, h, d.I, Tk, BN))
+        !make_tmap_bf16_2d(&prm.tmap_b, h, d.I, Tk, BN) ||
+        !make_tmap_bf16_2d(&prm.tmap_bh, h, d.I, Tk, BN / 2))
       return MOE_ERR_CUDA;
     prm.tmap_a1 = prm.tmap_a0;
     prm.offsets = offsets;
@@ -584,8 +522,7 @@ moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *
   if ((long)d.T * d.top_k >= 1024 && d.H % 256 == 0)
     return launch_experts_token_major(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h,
                                       status, stream);
-  switch (expert_bn(d)) {
-    case 16: return launch_experts_bn<16>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h, status, stream);
+  switch (expert_tile_rows(d)) {
     case 32: return launch_experts_bn<32>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h, status, stream);
     case 64: return launch_experts_bn<64>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h, status, stream);
     case 128: return launch_experts_bn<128>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial, h, status, stream);

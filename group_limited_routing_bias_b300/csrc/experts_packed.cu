@@ -448,13 +448,7 @@ template <class P>
 moe_status launch_fp4(const Fp4Params &prm, int grid, cudaStream_t stream) {
   constexpr int smem = smem_bytes_for<P>();
   static_assert(smem <= kSmemLimit, "shared memory budget");
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_smem_limit((const void *)tc_gemm_kernel<P>, smem) != MOE_OK) return MOE_ERR_CUDA;
   tc_gemm_kernel<P><<<grid, threads_for<P>(), smem, stream>>>(prm);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

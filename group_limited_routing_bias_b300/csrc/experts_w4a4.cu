@@ -515,15 +515,9 @@ moe_status launch_experts_w4a4(const moe_dims &d, const moe_experts &ex, const u
                                uint32_t *status, cudaStream_t stream) {
   const uint64_t Tk = (uint64_t)d.T * d.top_k;
   const uint64_t E = d.E, H = d.H, I = d.I;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(w4a4_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kW4SmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(w4a4_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kW4SmemBytes) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr = true;
-  }
+  if (ensure_smem_limit((const void *)w4a4_gemm_kernel<true>, kW4SmemBytes) != MOE_OK ||
+      ensure_smem_limit((const void *)w4a4_gemm_kernel<false>, kW4SmemBytes) != MOE_OK)
+    return MOE_ERR_CUDA;
   const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const int grid = device_sm_count();
 

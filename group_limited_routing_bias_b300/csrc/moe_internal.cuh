@@ -57,6 +57,16 @@ inline int expert_bn(const moe_dims &d) {
   return mean <= 16 ? 16 : mean <= 32 ? 32 : mean <= 64 ? 64 : mean <= 128 ? 128 : 256;
 }
 
+// Token rows per tile of the bf16 weights-on-M GEMMs: twice the mean class up
+// to 64, so an expert holding a few times the mean rows (common at decode,
+// where the selection bias concentrates the load) still streams its weights
+// once; a tile of at most half that loads a half-height activation box.  An
+// MMA with N <= 32 costs the same as N = 16.
+inline int expert_tile_rows(const moe_dims &d) {
+  const int bn = expert_bn(d);
+  return bn <= 32 ? 2 * bn : bn;
+}
+
 // ------------------------------------------------------------------ workspace
 
 struct WsLayout {
@@ -131,11 +141,18 @@ bool make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
 
 int device_sm_count();
 
+// Raises `kernel`'s dynamic shared memory limit to `bytes` on the current
+// device.  The attribute is per device, so this runs once per (kernel,
+// device) pair; safe to call from several host threads.
+moe_status ensure_smem_limit(const void *kernel, int bytes);
+
 // ------------------------------------------------------------------ launchers
 
+// logits (nullable): receives the fp32 logits [T, E] the selection is made from.
 moe_status launch_route(const moe_dims &d, const void *x, const float *w_router, const float *bias,
                         int32_t *topk_idx, float *topk_w, const RouterPlan &rp,
-                        __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream);
+                        __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream,
+                        float *logits = nullptr);
 
 // What the dispatch does with x after sorting: copy rows in bf16, copy them
 // as f16 (operands of the packed-weight GEMMs), or nothing (W4A4 quantises

@@ -256,14 +256,7 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
                           GatherMode gather) {
   const int Tk = d.T * d.top_k;
   const int nchunks = std::max(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
-  static bool attr_set = false;
-  const int scatter_smem = 32 * d.E * 4;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(permute_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             32 * 256 * 4) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  const int scatter_smem = 32 * d.E * 4;  // at most 32 KB (E <= 256): no opt-in needed
   if (nchunks == 1) {
     permute_small_kernel<<<1, kChunkThreads, scatter_smem, stream>>>(topk_idx, Tk, d.E,
                                                                      expert_offsets, slot_of,

@@ -54,12 +54,24 @@ __global__ void router_split_kernel(const float4 *__restrict__ w, uint4 *__restr
 }
 
 // logits partial sums: D[token, expert] over one K range of [x x x] . [hi mid lo]^T
+//
+// The tensor cores' fp32 accumulation does not round to nearest at every step:
+// over the 960 MMAs of a full K range (3 H = 15360 products) the logits of a
+// T = 16384 batch drifted by up to 1.2e-4 from the exact sums (mean 2e-5),
+// while split-K partials of 16 MMAs stayed within 2e-6.  So each CTA's K range
+// is cut into chunks of kChunkSlices 64-wide slices: every chunk starts a fresh
+// accumulator, and the epilogue adds the chunks in order, in fp32 with
+// round-to-nearest, into running sums kept in tensor memory next to the
+// accumulator; the last chunk's sum is the CTA's partial.
+constexpr int kChunkSlices = 8;  // 32 MMAs of K = 16 per accumulator
+
 template <int BN_>
 struct RouterLogits {
   static constexpr int BN = BN_;
   static constexpr int NA = 1;
   static constexpr int NBUF = 1;
   static constexpr int STAGES = 4;
+  static constexpr int EXTRA_TMEM_COLS = BN;  // running sums over the chunks
   struct Params {
     CUtensorMap tmap_x;   // bf16 [T, H], box {64, 128}
     CUtensorMap tmap_w3;  // bf16 [E, 3H], box {64, BN}
@@ -72,6 +84,7 @@ struct RouterLogits {
   };
   struct Tile {
     int m0, kbeg, kend, split;
+    bool first, last;  // first and last chunk of the CTA's K range
   };
   static constexpr bool CONVERT = false;
   static constexpr bool F16 = false;
@@ -80,11 +93,23 @@ struct RouterLogits {
   static constexpr int TX_BYTES = StageGeom<BN, NA>::kOperandBytes;
   __device__ static void convert(const Params &, const Tile &, int, uint8_t *, int) {}
   __device__ static void prologue(const Params &, Sched &) {}
-  __device__ static int num_tiles(const Params &, const Sched &) { return gridDim.x; }
+  // K range of this CTA's split
+  __device__ static int split_begin(const Params &p, int s) { return (int)((long)p.ksteps * s / p.ksplit); }
+  // One M tile per CTA (grid.x = M tiles, grid.y = splits); its tiles are the
+  // chunks of its K range, t = blockIdx.x + chunk * gridDim.x.
+  __device__ static int num_tiles(const Params &p, const Sched &) {
+    const int s = blockIdx.y;
+    const int nk = split_begin(p, s + 1) - split_begin(p, s);
+    return gridDim.x * ((nk + kChunkSlices - 1) / kChunkSlices);
+  }
   __device__ static Tile tile(const Params &p, const Sched &, int t) {
     const int s = blockIdx.y;
-    return Tile{t * kTileM, (int)((long)p.ksteps * s / p.ksplit),
-                (int)((long)p.ksteps * (s + 1) / p.ksplit), s};
+    const int kb = split_begin(p, s), ke = split_begin(p, s + 1);
+    const int g = (int)gridDim.x;
+    const int chunk = t / g;
+    const int cb = kb + chunk * kChunkSlices;
+    const int ce = min(cb + kChunkSlices, ke);
+    return Tile{(t % g) * kTileM, cb, ce, s, chunk == 0, ce == ke};
   }
   __device__ static int num_k(const Params &, const Tile &t) { return t.kend - t.kbeg; }
   __device__ static void load(const Params &p, const Tile &t, int k, uint8_t *stage, uint64_t *bar) {
@@ -95,12 +120,26 @@ struct RouterLogits {
   }
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     const int token = t.m0 + row;
+    const uint32_t run = taddr + BN;  // NBUF == 1: the running sums follow the accumulator
+    bool stored = false;
     for (int c = 0; c < BN; c += 32) {
       if (c >= p.E) break;
       uint32_t r[32];
       tmem_ld32(taddr + c, r);
-      tmem_wait_ld();
-      if (token < p.T) {
+      if (!t.first) {
+        uint32_t a[32];
+        tmem_ld32(run + c, a);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          r[j] = __float_as_uint(__fadd_rn(__uint_as_float(a[j]), __uint_as_float(r[j])));
+      } else {
+        tmem_wait_ld();
+      }
+      if (!t.last) {
+        tmem_st32(run + c, r);
+        stored = true;
+      } else if (token < p.T) {
         float4 *dst = reinterpret_cast<float4 *>(p.partial + ((size_t)t.split * p.T + token) * p.E + c);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -108,6 +147,7 @@ struct RouterLogits {
                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
       }
     }
+    if (stored) tmem_wait_st();
   }
 };
 
@@ -116,6 +156,7 @@ struct RouterLogits {
 struct TopkArgs {
   const float *partial;  // [ksplit, T, E]
   const float *bias;     // [E]
+  float *logits;         // [T, E] or null: the summed logits the selection uses
   int32_t *topk_idx;     // [T, k]
   float *topk_w;         // [T, k]
   int T, E, n_group, topk_group, top_k, ksplit;
@@ -167,7 +208,10 @@ __global__ void __launch_bounds__(256) router_topk_kernel(TopkArgs a) {
       }
     }
 #pragma unroll
-    for (int j = 0; j < TPB; ++j) logits_s[j][e] = acc[j];
+    for (int j = 0; j < TPB; ++j) {
+      logits_s[j][e] = acc[j];
+      if (a.logits && e < a.E && t0 + j < a.T) a.logits[(size_t)(t0 + j) * a.E + e] = acc[j];
+    }
   }
   __syncthreads();
   if ((threadIdx.x >> 5) >= TPB) return;
@@ -302,13 +346,7 @@ static moe_status launch_router_gemm(const RouterPlan &rp, const void *x, const 
   prm.ksplit = rp.ksplit;
   prm.status = status;
   constexpr int smem = smem_bytes_for<P>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_smem_limit((const void *)tc_gemm_kernel<P>, smem) != MOE_OK) return MOE_ERR_CUDA;
   dim3 grid((rp.T + kTileM - 1) / kTileM, rp.ksplit);
   tc_gemm_kernel<P><<<grid, 256, smem, stream>>>(prm);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -316,7 +354,8 @@ static moe_status launch_router_gemm(const RouterPlan &rp, const void *x, const 
 
 moe_status launch_route(const moe_dims &d, const void *x, const float *w_router, const float *bias,
                         int32_t *topk_idx, float *topk_w, const RouterPlan &rp,
-                        __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream) {
+                        __nv_bfloat16 *w3, float *partial, uint32_t *status, cudaStream_t stream,
+                        float *logits) {
   {
     const size_t n = (size_t)d.E * d.H / 8;
     const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
@@ -334,6 +373,7 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
   TopkArgs a;
   a.partial = partial;
   a.bias = bias;
+  a.logits = logits;
   a.topk_idx = topk_idx;
   a.topk_w = topk_w;
   a.T = d.T;

@@ -65,6 +65,9 @@
 //   static uint32_t tx_bytes(const Params&, const Tile&)  (optional: the bytes load()
 //                                          brings for that tile, when not TX_BYTES)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
+//   static constexpr int EXTRA_TMEM_COLS;  (optional, default 0: tensor-memory
+//                                          columns after the NBUF accumulators,
+//                                          at taddr - buf * NA * BN + NBUF * NA * BN)
 //   CONVERT problems load the operand ring's activation tile with load() and the
 //   raw ring with
 //   static void load_raw(const Params&, const Tile&, int k, uint8_t *raw, uint64_t *raw_bar)
@@ -186,6 +189,17 @@ template <class P>
 struct HasLastCta<P, std::void_t<decltype(P::last_cta(std::declval<const typename P::Params &>()))>>
     : std::true_type {};
 
+// Tensor-memory columns a problem keeps beyond its accumulators (optional
+// P::EXTRA_TMEM_COLS, default 0), at [NBUF * NA * BN, + EXTRA) of every lane.
+template <class P, class = void>
+struct ExtraTmemOf {
+  static constexpr int value = 0;
+};
+template <class P>
+struct ExtraTmemOf<P, std::void_t<decltype(P::EXTRA_TMEM_COLS)>> {
+  static constexpr int value = P::EXTRA_TMEM_COLS;
+};
+
 template <class P>
 __host__ __device__ constexpr int threads_for() {
   return P::CONVERT ? 256 + 32 * ConvertWarpsOf<P>::value : 256;
@@ -220,9 +234,9 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
     tc_gemm_kernel(const __grid_constant__ typename P::Params p) {
   constexpr int STAGE = stage_bytes_of<P>();
   constexpr uint32_t kAccCols = P::NA * P::BN;
-  constexpr uint32_t kTmemCols = tmem_cols_pow2(P::NBUF * kAccCols);
+  constexpr uint32_t kTmemCols = tmem_cols_pow2(P::NBUF * kAccCols + ExtraTmemOf<P>::value);
   constexpr uint32_t kIdesc = P::F16 ? umma_idesc_f16(kTileM, P::BN) : umma_idesc_bf16(kTileM, P::BN);
-  static_assert(P::NBUF * kAccCols <= 512, "accumulators exceed tensor memory");
+  static_assert(P::NBUF * kAccCols + ExtraTmemOf<P>::value <= 512, "tensor memory overflow");
   constexpr int CG = CGroupsOf<P>::value;
   constexpr int kGroupWarps = ConvertWarpsOf<P>::value / CG;
   static_assert(ConvertWarpsOf<P>::value % CG == 0, "converter groups must split the converter warps");

@@ -180,6 +180,19 @@ moe_status moe_route(const moe_dims *dims, const void *x, const float *w_router,
                      size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_route with one more output: logits fp32 [T, E] receives the router
+ * logits x . w_router^T from which the selection above was made, exactly the
+ * values the sigmoid is applied to (the same fp32 sums, in the same order).
+ * Routing outputs are identical to moe_route's.  For inspection of the
+ * router and for losses on its logits; the pages define the logit as the
+ * router's dot product ("Reflection Releases Beam ...", section "Where Beam
+ * Saves ...": sigmoid scores over the router's output).  Workspace: MOE_OP_ROUTE.
+ */
+moe_status moe_route_logits(const moe_dims *dims, const void *x, const float *w_router,
+                            const float *bias, int32_t *topk_idx, float *topk_w, float *logits,
+                            void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Dispatch: sorts the T*k (token, slot) entries by expert, stably (entries of
  * one expert keep ascending t*k + j order), and gathers x rows into that order.
  * (The pages: tokens must reach the experts they selected — "Beam Turns
@@ -217,7 +230,13 @@ moe_status moe_combine(const moe_dims *dims, const void *y_partial, const int32_
 
 /*
  * The whole block: moe_route, moe_permute, moe_experts_swiglu and moe_combine
- * in sequence on `stream`, with every intermediate in the workspace.
+ * in sequence on `stream`, with every intermediate in the workspace.  The
+ * block as the pages state it: "Hugging Face releases Beam ...", third
+ * paragraph (256 experts per layer, each a SwiGLU MLP of intermediate size
+ * 2,560; the top 8 experts from the top 4 of 8 groups of 32), and "Reflection
+ * Releases Beam ...", section "Where Beam Saves and Where the Memory Bill
+ * Comes In" (sigmoid router, outputs normalised and scaled by 2.5, no shared
+ * expert).
  * topk_idx / topk_w may be NULL; when given they receive the routing.
  * Workspace: MOE_OP_FORWARD.
  */
@@ -317,11 +336,17 @@ moe_status moe_pack_fp8(int E, int N, int K, const uint8_t *q, uint8_t *dst, moe
  *   scratch (per-chunk expert counts and bases) lives in one 1 MiB device
  *   array inside the library, which every GPU that loads the library holds
  *   until the process exits.
- *   Limit: 256 + 2 * 4 * E * ceil(T*k / 4096) bytes must fit in 1 MiB, i.e.
- *   T*k <= 2,093,056 entries at E = 256; larger calls return
- *   MOE_ERR_UNSUPPORTED before launching anything.
+ *   Limit: 256 + 2 * round_up(4 * E * ceil(T*k / 4096), 256) bytes must fit
+ *   in 1 MiB (a 256-byte header, then two tables, each rounded up to 256
+ *   bytes), i.e. T*k <= 2,093,056 entries at E = 256 and <= 16,769,024 at
+ *   E = 32; larger calls return MOE_ERR_UNSUPPORTED before launching
+ *   anything.
  *   The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
+ *   that device current and keeps it for the life of the process; make that
+ *   first call before any stream capture.  The address belongs to the
+ *   device's primary context: do not call this entry point from another
+ *   driver context, or after cudaDeviceReset (which may reload the library's
+ *   device code at another address).
  *   All calls share the one array: calls that overlap on the GPU (other
  *   streams, other host threads) race and corrupt each other's results.
  *   Out-of-range expert indices are dropped as in moe_permute, but no status

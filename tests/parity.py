@@ -21,14 +21,31 @@ from dataclasses import dataclass, field
 import numpy as np
 
 TIE_EPS = 1e-5
-# Routed weights: the GPU accumulates each logit's 3 * H exact products in fp32
-# in a different order than the oracle's fp64 sum, a difference of order
-# 1e-6 in the logit.  That moves s = sigmoid(logit) by up to about
-# s (1 - s) 1e-6, which for the smaller chosen scores (s ~ 0.1) is ~1e-5 of s
-# relative; the weight 2.5 s / sum(s) inherits it.  2e-5 bounds that with
-# margin and is still far below any reading error (biased-score weights, a
-# missing 2.5, a dropped expert all move weights by whole percents).
-W_RTOL = 2e-5
+
+# Router logits.  The GPU sums each logit's 3 * H exact products (bf16 x times
+# the three exact bf16 parts of the fp32 router weight) on the tensor cores in
+# chunks of 32 MMAs, and adds the chunks in fp32 with round-to-nearest; the
+# oracle sums in fp64 and rounds once to fp32.  LOGIT_ATOL bounds
+# |GPU logit - oracle logit|; it is asserted directly on the logits
+# moe_route_logits returns (tests/test_gpu_parity.py: all 4.2 M logits of the
+# T = 16384 workload, the K-split decode batch and a ragged tiny batch).  The
+# largest difference measured on B300 is LOGIT_MEASURED (T = 16384; 1.9e-6 at
+# decode); the bar is about twice that.  (Accumulating the whole K range of
+# 960 MMAs in one tensor-core accumulator gave 1.2e-4: its fp32 accumulation
+# does not round to nearest at every step.)
+LOGIT_MEASURED = 4.3e-6
+LOGIT_ATOL = 1e-5
+
+# Routed weights w_j = r s_j / sum_i s_i with s = sigmoid(logit).  A logit
+# error d moves ln s by (1 - s) d, at most d, so ln w_j moves by at most
+# 2 max|d| (d ln s_j minus d ln sum s, each at most max|d|).  fp32 rounding
+# adds, relative: the GPU's sigmoid (expf within 2 ulp, the add and the IEEE
+# division: 3 ulp), the sum of 8 scores (7 roundings), the product and the
+# division (2), and the oracle's own rounding of s and w (2); with ulp = 2^-23
+# that is about 1.5e-6.  Any reading error (weights from biased scores, a
+# missing 2.5, a dropped expert) moves weights by whole percents.
+W_ROUND = 1.5e-6
+W_RTOL = 2 * LOGIT_ATOL + W_ROUND
 BF16_MAX_ERR = 2e-2      # max |err| <= 2e-2 * max |ref|
 BF16_REL_FROB = 5e-3     # ||err|| <= 5e-3 * ||ref||
 NVFP4_REL_FROB = 3e-2
@@ -163,3 +180,48 @@ def output_errors(y_gpu, y_ref) -> OutputErrors:
     err = a - b
     return OutputErrors(float(np.abs(err).max()), float(np.abs(b).max()),
                         float(np.linalg.norm(err) / np.linalg.norm(b)))
+
+
+def stratified_tokens(idx, E: int, tile_rows: int = 128, n_random: int = 32, seed: int = 0):
+    """Tokens whose outputs a sampled parity check compares, at sizes where the
+    oracle cannot evaluate every token.  Built from the routing the GPU used
+    (idx int32 [T, k], all in [0, E)) and the dispatch's stable order (rows
+    expert-major, entries t*k + j ascending inside an expert):
+      - for every touched expert, the tokens of its first permuted row, of the
+        first row of its last tile of tile_rows rows, and of its last row (the
+        boundary rows of every expert's ragged final tile);
+      - for the most-loaded expert, the first and last row of every tile;
+      - n_random more tokens drawn with the seed.
+    Every touched expert thus contributes to at least one compared output."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    flat = idx.ravel()
+    order = np.argsort(flat, kind="stable")  # permuted row -> entry
+    counts = np.bincount(flat, minlength=E)
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    rows = []
+    for e in np.nonzero(counts)[0]:
+        n, o = int(counts[e]), int(offs[e])
+        rows += [o, o + (n - 1) // tile_rows * tile_rows, o + n - 1]
+    heavy = int(np.argmax(counts))
+    for r0 in range(0, int(counts[heavy]), tile_rows):
+        rows += [offs[heavy] + r0, offs[heavy] + min(r0 + tile_rows, int(counts[heavy])) - 1]
+    toks = set((order[np.asarray(rows, np.int64)] // k).tolist())
+    rng = np.random.default_rng(seed)
+    toks |= set(rng.choice(T, min(n_random, T), replace=False).tolist())
+    out = np.array(sorted(toks), dtype=np.int64)
+    assert set(np.unique(idx[out])) == set(np.unique(flat)), "a touched expert has no sampled row"
+    return out
+
+
+def sample_tokens(sample, idx, E: int):
+    """Tokens a parity check compares: every token (sample None), the
+    stratified sample over the GPU's routing (sample "stratified"), or the
+    given indices."""
+    T = np.asarray(idx).shape[0]
+    if sample is None:
+        return np.arange(T)
+    if isinstance(sample, str):
+        assert sample == "stratified"
+        return stratified_tokens(idx, E, seed=T)
+    return np.asarray(sample)

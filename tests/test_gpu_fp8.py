@@ -8,7 +8,8 @@ import torch
 
 import moe_inputs as mi
 import oracle
-from parity import compare_routing, output_errors, reference_routing
+from parity import (compare_routing, output_errors, reference_routing,
+                    sample_tokens)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -47,7 +48,7 @@ class Fp8Case:
                 M(self.qd[e].cpu().numpy(), self.rd[e].cpu().numpy()))
 
 
-def check(lib, case, sample=None):
+def forward(lib, case):
     c = case.cfg
     d = lib.dims_of(c)
     ws = lib.alloc_workspace(d, lib.MOE_OP_FORWARD, lib.MOE_W_FP8)
@@ -56,13 +57,18 @@ def check(lib, case, sample=None):
     w = torch.empty(c.T, c.top_k, dtype=torch.float32, device=DEV)
     lib.moe_forward(d, case.x, case.wr, case.b, case.experts(lib), y, ws, idx, w)
     assert lib.workspace_status(ws) == 0
-    idx, w = idx.cpu().numpy(), w.cpu().numpy()
+    return y, idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check(lib, case, sample=None):
+    c = case.cfg
+    y, idx, w = forward(lib, case)
     orc = oracle.route(mi.bf16_bits(case.x_h), case.wr_h.numpy(), case.b_h.numpy(), c.n_group,
                        c.topk_group, c.top_k, c.routed_scale, details=True)
     rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
     assert rep.ok, (rep, rep.mismatch_info)
     ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
-    tokens = np.arange(c.T) if sample is None else np.asarray(sample)
+    tokens = sample_tokens(sample, idx, c.E)
     y_ref = oracle.experts_forward(mi.bf16_bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
     err = output_errors(y.double().cpu().numpy()[tokens], y_ref)
     print(f"\n[{c.name} T={c.T}] routing {rep}; output {err} over {len(tokens)} tokens")
@@ -76,22 +82,18 @@ def test_fp8_tiny(lib, T):
     check(lib, Fp8Case(mi.CONFIGS["tiny"], T=T))
 
 
-@pytest.mark.parametrize("T,n_sample", [(64, None), (16384, 48)])
-def test_fp8_beam(lib, T, n_sample):
-    case = Fp8Case(mi.CONFIGS["fp8"], T=T)
-    sample = None if n_sample is None else np.sort(
-        np.random.default_rng(T).choice(T, n_sample, replace=False))
-    check(lib, case, sample)
+@pytest.mark.parametrize("T,sample", [(64, None), (16384, "stratified")])
+def test_fp8_beam(lib, T, sample):
+    check(lib, Fp8Case(mi.CONFIGS["fp8"], T=T), sample)
 
 
-@pytest.mark.parametrize("name,T,n_sample", [("tiny", 5, None), ("tiny", 64, None), ("tiny", 2048, None),
-                                              ("fp8", 64, None), ("fp8", 16384, 48)])
-def test_fp8_tiled(lib, name, T, n_sample):
+@pytest.mark.parametrize("name,T,sample", [("tiny", 5, None), ("tiny", 64, None),
+                                            ("tiny", 2048, None), ("fp8", 64, None),
+                                            ("fp8", 16384, "stratified")])
+def test_fp8_tiled(lib, name, T, sample):
     """Weights in the tiled layout (moe_pack_fp8), on both GEMM paths: parity
     with the oracle, and the row-major forward's output bit for bit."""
     case = Fp8Case(mi.CONFIGS[name], T=T)
-    sample = None if n_sample is None else np.sort(
-        np.random.default_rng(T).choice(T, n_sample, replace=False))
     y_rm = check(lib, case, sample)
     case.tiled = True
-    assert torch.equal(check(lib, case, sample), y_rm)
+    assert torch.equal(forward(lib, case)[0], y_rm)

@@ -1,10 +1,14 @@
 """GPU parity: every stage of the CUDA path, called through the C ABI, against
 the CPU oracle on the same seeded inputs.
 
-Bars: routing indices bit-exact except counted near ties (tests/parity.py),
-weights within 2e-6 relative; dispatch bit-exact against a stable sort;
-combine bit-exact against an fp32 sum in k order; outputs within
-max|err| <= 2e-2 * max|ref| and relative Frobenius error <= 5e-3.
+Bars: router logits within LOGIT_ATOL of the oracle's (asserted on every
+logit); routing indices bit-exact except counted near ties (tests/parity.py);
+weights within W_RTOL relative, derived there from the logit bound;
+dispatch bit-exact against a stable sort; combine bit-exact against an fp32
+sum in k order; outputs within max|err| <= 2e-2 * max|ref| and relative
+Frobenius error <= 5e-3, on every token up to mid-size batches and, at
+T = 16384, on a stratified sample that gives every touched expert compared
+rows and includes the boundary rows of every expert's last tile.
 """
 import numpy as np
 import pytest
@@ -12,7 +16,8 @@ import torch
 
 import moe_inputs as mi
 import oracle
-from parity import (compare_routing, output_errors, reference_routing)
+from parity import (LOGIT_ATOL, W_RTOL, compare_routing, output_errors, reference_routing,
+                    stratified_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -82,6 +87,36 @@ def test_route(lib, name, T):
     case = Case(mi.CONFIGS[name], T=T, weights=False)
     idx, w = gpu_route(lib, case)
     check_routing(case, case.oracle_route(), idx, w)
+
+
+@pytest.mark.parametrize("name,T", [("decode", 64), ("tiny", 333), ("prefill", 16384)])
+def test_route_logits_within_bound(lib, name, T):
+    """The fp32 logits the selection is made from (moe_route_logits) against the
+    oracle's fp64 sums rounded to fp32, every logit: the measured difference
+    is what bounds the routed weights' error (W_RTOL).  decode T=64 adds
+    K-split partial sums; T=16384 runs one K range per tile.  The routing
+    outputs equal moe_route's bit for bit."""
+    case = Case(mi.CONFIGS[name], T=T, weights=False)
+    c = case.cfg
+    d = lib.dims_of(c)
+    ws = lib.alloc_workspace(d, lib.MOE_OP_ROUTE)
+    idx = torch.full((c.T, c.top_k), -1, dtype=torch.int32, device=DEV)
+    w = torch.zeros((c.T, c.top_k), dtype=torch.float32, device=DEV)
+    logits = torch.full((c.T, c.E), float("nan"), dtype=torch.float32, device=DEV)
+    lib.moe_route_logits(d, case.x, case.wr, case.b, idx, w, logits, ws)
+    assert lib.workspace_status(ws) == 0
+    orc = case.oracle_route()
+    got = logits.cpu().numpy().astype(np.float64)
+    diff = np.abs(got - orc.logits.astype(np.float64))
+    print(f"\n[{c.name} T={c.T}] max |logit - oracle| = {diff.max():.3e} "
+          f"(mean {diff.mean():.2e}, max |logit| {np.abs(got).max():.2f}); bound {LOGIT_ATOL:.1e}, "
+          f"weights bound {W_RTOL:.2e}")
+    assert np.isfinite(got).all()
+    assert diff.max() <= LOGIT_ATOL
+    i2, w2 = gpu_route(lib, case)
+    np.testing.assert_array_equal(idx.cpu().numpy(), i2)
+    np.testing.assert_array_equal(w.cpu().numpy(), w2)
+    check_routing(case, orc, i2, w2)
 
 
 def test_route_all_ties_pick_lowest(lib):
@@ -170,12 +205,17 @@ def forward(lib, case, sample=None):
 
 
 def check_forward(lib, case, sample=None):
+    """sample: None (every token), "stratified" (tests/parity.py's
+    stratified_tokens over the GPU's routing) or explicit token indices."""
     c = case.cfg
     y, idx, w = forward(lib, case)
     orc = case.oracle_route()
     rep = check_routing(case, orc, idx, w)
     ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
-    tokens = np.arange(c.T) if sample is None else np.asarray(sample)
+    if isinstance(sample, str):
+        tokens = stratified_tokens(idx, c.E, seed=c.T)
+    else:
+        tokens = np.arange(c.T) if sample is None else np.asarray(sample)
     y_ref = oracle.experts_forward(bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
     err = output_errors(y[tokens], y_ref)
     print(f"[{c.name} T={c.T}] output: {err} over {len(tokens)} tokens")
@@ -203,6 +243,19 @@ def test_forward_tiny_skewed_token_major(lib):
     assert load.max() > 3 * load.mean()
 
 
+def test_forward_tiny_skewed_weights_on_m(lib):
+    """Weights-on-M path (T*k < 1024) with a strongly skewed load: experts of a
+    few rows (half-height activation box), of up to one tile, and of several
+    tiles; every output compared."""
+    c = mi.CONFIGS["tiny"].with_T(200)
+    case = Case(c)
+    case.b_h = mi.zipf_bias(c.E, 0.15, seed=5)
+    case.b = case.b_h.to(DEV)
+    y, idx, _ = check_forward(lib, case)
+    load = np.bincount(idx.ravel(), minlength=c.E)
+    assert load.max() > 64 and (load[load > 0] <= 32).any()
+
+
 def test_forward_decode_full(lib):
     """The decode workload in the launch configuration the benchmark times."""
     check_forward(lib, Case(mi.CONFIGS["decode"]))
@@ -218,15 +271,16 @@ def test_forward_beam_mid_batch_sampled(lib, T):
 
 
 def test_forward_prefill_sampled(lib):
-    rng = np.random.default_rng(0)
-    case = Case(mi.CONFIGS["prefill"])
-    check_forward(lib, case, sample=np.sort(rng.choice(case.cfg.T, 96, replace=False)))
+    """T=16384, every touched expert's first row, last-tile boundary rows and
+    last row compared (stratified sample)."""
+    check_forward(lib, Case(mi.CONFIGS["prefill"]), sample="stratified")
 
 
 def test_forward_skewed_sampled(lib):
-    rng = np.random.default_rng(1)
+    """Skewed load (max ~8x mean): the stratified sample adds the first and last
+    row of every tile of the most-loaded expert."""
     case = Case(mi.CONFIGS["skewed"])
-    y, idx, _ = check_forward(lib, case, sample=np.sort(rng.choice(case.cfg.T, 96, replace=False)))
+    y, idx, _ = check_forward(lib, case, sample="stratified")
     load = np.bincount(idx.ravel(), minlength=256)
     assert load.max() >= 6 * load.mean()
 

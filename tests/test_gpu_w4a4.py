@@ -15,7 +15,8 @@ import torch
 
 import moe_inputs as mi
 import oracle
-from parity import NVFP4_REL_FROB, compare_routing, output_errors, reference_routing
+from parity import (NVFP4_REL_FROB, compare_routing, output_errors, reference_routing,
+                    sample_tokens)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -76,7 +77,7 @@ def check(lib, case, sample=None):
     rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
     assert rep.ok, (rep, rep.mismatch_info)
     ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
-    tokens = np.arange(c.T) if sample is None else np.asarray(sample)
+    tokens = sample_tokens(sample, idx, c.E)
     y_ref = oracle.experts_forward(mi.bf16_bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens,
                                    a4=A4)
     err = output_errors(y.double().cpu().numpy()[tokens], y_ref)
@@ -132,13 +133,13 @@ def test_w4a4_tiny(lib, T):
     check(lib, A4Case(TINY4, T=T))
 
 
-@pytest.mark.parametrize("T,n_sample", [(1, None), (64, None), (1024, 64), (16384, 48)])
-def test_w4a4_beam(lib, T, n_sample):
-    case = A4Case(mi.CONFIGS["nvfp4"], T=T)
-    sample = None
-    if n_sample is not None:
-        sample = np.sort(np.random.default_rng(T).choice(T, n_sample, replace=False))
-    check(lib, case, sample)
+@pytest.mark.parametrize("T,sample", [(1, None), (64, None), (1024, "stratified"),
+                                      (16384, "stratified")])
+def test_w4a4_beam(lib, T, sample):
+    """The four batch sizes of the NVFP4 workload with NVFP4 activations; from
+    T=1024 every touched expert's first row, last-tile boundary rows and last
+    row are compared."""
+    check(lib, A4Case(mi.CONFIGS["nvfp4"], T=T), sample)
 
 
 def test_w4a4_experts_entry_point_matches_forward(lib):
@@ -199,8 +200,7 @@ def test_w4a4_beam_skewed_sampled(lib):
                        routed_scale=base.routed_scale, bias=base.bias, weights="nvfp4",
                        zipf_alpha=base.zipf_alpha)
     case = A4Case(cfg)
-    sample = np.sort(np.random.default_rng(7).choice(cfg.T, 48, replace=False))
-    check(lib, case, sample)
+    check(lib, case, "stratified")
     _, idx, _ = forward(lib, case)
     load = np.bincount(idx.ravel(), minlength=cfg.E)
     assert load.max() >= 6 * load.mean()
