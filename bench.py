@@ -223,12 +223,36 @@ FP8_EXPERT_BYTES = 3 * 5120 * 2560 + (2 * 2560 + 5120) * 4              # e4m3 c
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense fp4 / bf16 tensor rate of B300
 
 
+def token_major_schedule(counts, H, I, sms):
+    """Load figures of the token-major expert GEMMs' static schedule (CTA b takes
+    tiles b, b + grid, ...; a tile is 128 token rows of one expert against 128
+    gate + 128 up or 256 down features) for expert loads `counts`: rows per
+    expert, tiles and waves per GEMM, the spread of tiles over CTAs, and the
+    share of MMA rows that are padding (a ragged tile costs a full one)."""
+    counts = np.asarray(counts, np.int64)
+    token_tiles = (counts + 127) // 128
+    out = {"rows_per_expert_max": int(counts.max()), "rows_per_expert_mean": float(counts.mean()),
+           "max_over_mean": float(counts.max() / counts.mean()),
+           "experts_touched": int((counts > 0).sum()),
+           "padded_row_frac": float(1 - counts.sum() / (128 * token_tiles.sum()))}
+    for name, nf in (("gate_up", I // 128), ("down", H // 256)):
+        n = int(token_tiles.sum() * nf)
+        grid = max(1, min(sms, n))
+        per = np.bincount(np.arange(n) % grid, minlength=grid)
+        out[name] = {"tiles": n, "grid": grid, "waves": n / grid, "tiles_per_cta_max": int(per.max()),
+                     "tiles_per_cta_min": int(per.min()),
+                     "busy_frac": float(per.sum() / (per.max() * grid))}
+    return out
+
+
 def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
-    """Prefill (T=16384) as a secondary figure, with clocks sampled over its timed
-    steps.  Its GEMMs run inside a loop of ~10 ms steps, so when the samples
-    show the power cap active (sw_power_cap) or the clocks below 90% of max,
-    the peak it is compared with is the sustained one (cuBLAS back to back under
-    the same cap), else the burst one; both fractions are printed."""
+    """Prefill (T=16384) or the skewed workload as a secondary figure, with
+    clocks sampled over its timed steps.  Its GEMMs run inside a loop of ~10 ms
+    steps, so when the samples show the power cap active (sw_power_cap) or the
+    clocks below 90% of max, the peak it is compared with is the sustained one
+    (cuBLAS back to back under the same cap), else the burst one; both
+    fractions are printed.  The load of the expert GEMMs' tile schedule
+    (token_major_schedule) comes with it."""
     pw = Workload(lib, cfg, weights, dev)
     for _ in range(2):
         pw.forward(lib)
@@ -252,6 +276,9 @@ def prefill_figures(lib, cfg, weights, dev, flush, peaks, steps):
            "frac_of_bf16_peak": tflops / peak,
            "frac_of_burst_peak": tflops / peaks["bf16"],
            "frac_of_sustained_peak": tflops / peaks["bf16_sust"], "clocks": clocks}
+    counts = np.bincount(pw.idx.cpu().numpy().ravel(), minlength=cfg.E)
+    out["schedule"] = token_major_schedule(counts, cfg.H, cfg.I,
+                                           torch.cuda.get_device_properties(dev).multi_processor_count)
     del pw
     torch.cuda.empty_cache()
     return out
@@ -564,6 +591,12 @@ def main():
         prefill = prefill_figures(lib, mi.CONFIGS["prefill"], weights, dev, flush, peaks,
                                   args.prefill_steps)
 
+    # ---- skewed load (max ~8x mean rows per expert), same shapes and weights
+    skewed = None
+    if not args.no_prefill:
+        skewed = prefill_figures(lib, mi.CONFIGS["skewed"], weights, dev, flush, peaks,
+                                 args.prefill_steps)
+
     # ---- packed experts (the decode weights packed to NVFP4 and to FP8), decode and prefill
     nvfp4 = fp8 = None
     if not args.no_nvfp4:
@@ -596,7 +629,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "ms_per_step_eager": eager_ms,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": launches_per_forward(cfg.T, cfg.top_k) * args.steps, "stages_ms": stages, "prefill": prefill, "nvfp4": nvfp4, "fp8": fp8,
+        "gpu_launches": launches_per_forward(cfg.T, cfg.top_k) * args.steps, "stages_ms": stages, "prefill": prefill, "skewed": skewed, "nvfp4": nvfp4, "fp8": fp8,
     }
     print(json.dumps(line))
     if dist is not None:
