@@ -270,6 +270,9 @@ moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts, 
     return launch_experts_w4a4(*dims, *experts, xq, xs, expert_offsets, row_src, topk_w, y_partial,
                                at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status_word(ws), s);
   }
+  if (experts->dtype != MOE_W_BF16 && packed_wt_applies(*dims))
+    return launch_experts_packed_wt(*dims, *experts, x_perm, expert_offsets, row_src, topk_w,
+                                    y_partial, at<__nv_bfloat16>(ws, L.h), status_word(ws), s);
   if (experts->dtype != MOE_W_BF16) {
     void *x16 = at<void>(ws, L.x16);
     const size_t n = (size_t)dims->T * dims->top_k * dims->H;
@@ -304,7 +307,11 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   const moe_dims &d = *dims;
   const WsLayout L = ws_layout(d, MOE_OP_FORWARD, experts->dtype);
   const bool a4 = experts->dtype == MOE_W_NVFP4_A4;
-  const bool fp4 = experts->dtype != MOE_W_BF16 && !a4;  // packed weights, f16 activations
+  const bool packed = experts->dtype != MOE_W_BF16 && !a4;
+  // packed weights: small and mid-size batches dequantise into tensor memory
+  // with bf16 activations; large ones run the token-major GEMMs on f16 ones
+  const bool packed_wt = packed && packed_wt_applies(d);
+  const bool fp4 = packed && !packed_wt;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t *idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
   float *w = topk_w ? topk_w : at<float>(ws, L.topk_w);
@@ -316,8 +323,9 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   int32_t *offsets = at<int32_t>(ws, L.offsets);
   int32_t *slot_of = at<int32_t>(ws, L.slot_of);
   int32_t *row_src = at<int32_t>(ws, L.row_src);
-  // with NVFP4 or FP8 weights the gather writes x_perm in f16, the GEMMs'
-  // operand type; W4A4 quantises each token once and writes it to its slots
+  // the gather writes x_perm in the GEMMs' operand type: bf16, or f16 for the
+  // token-major packed-weight GEMMs; W4A4 quantises each token once and
+  // writes it to its slots
   const GatherMode gm = a4 ? kGatherNone : fp4 ? kGatherF16 : kGatherBf16;
   if ((st = launch_permute(d, idx, x, x_perm, offsets, slot_of, row_src, at<int32_t>(ws, L.counts),
                            at<int32_t>(ws, L.bases), status, s, gm)) != MOE_OK)
@@ -330,7 +338,10 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
       return st;
     st = launch_experts_w4a4(d, *experts, xq, xs, offsets, row_src, w, y_partial,
                              at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status, s);
-  } else if (fp4)
+  } else if (packed_wt)
+    st = launch_experts_packed_wt(d, *experts, x_perm, offsets, row_src, w, y_partial,
+                                  at<__nv_bfloat16>(ws, L.h), status, s);
+  else if (fp4)
     st = launch_experts_fp4(d, *experts, x_perm, offsets, row_src, w, y_partial, at<void>(ws, L.h),
                             status, s);
   else

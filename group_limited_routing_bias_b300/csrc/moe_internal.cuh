@@ -194,6 +194,16 @@ moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const vo
                               const float *topk_w, void *y_partial, void *h16, uint32_t *status,
                               cudaStream_t stream);
 
+// NVFP4 or FP8 weights with bf16 x_perm and h [Tk, I]: weights dequantised
+// into tensor memory, token rows on the MMA's N side (experts_packed_wt.cu).
+// Used while the token tiles hold at most kPackedWtMaxRows rows.
+constexpr int kPackedWtMaxRows = 64;
+bool packed_wt_applies(const moe_dims &d);
+moe_status launch_experts_packed_wt(const moe_dims &d, const moe_experts &ex, const void *x_perm,
+                                    const int32_t *expert_offsets, const int32_t *row_src,
+                                    const float *topk_w, void *y_partial, __nv_bfloat16 *h,
+                                    uint32_t *status, cudaStream_t stream);
+
 // bf16 [E, N, K] -> MMA-tiled layout (see moe_pack_bf16 in beam_moe.h).
 moe_status launch_pack_bf16(int E, int N, int K, const void *src, void *dst, cudaStream_t stream);
 

@@ -5,7 +5,8 @@
 // with every operand K-major bf16 staged by TMA in 64-wide K slices with the
 // 128-byte swizzle.
 //   warp 0 lane 0 : TMA producer, STAGES-deep shared-memory ring
-//   warp 1 lane 0 : MMA issuer (tcgen05.mma, M=128, N=BN, K=16 per instruction)
+//   warp 1        : MMA issuer (tcgen05.mma, M=128, N=BN, K=16 per instruction),
+//                   the whole warp converged, one elected lane issuing
 //   warp 2        : tensor-memory allocation / release
 //   warps 4..7    : epilogue; warp 4+q reads accumulator rows 32q..32q+31
 // The accumulators are double-buffered in tensor memory when they fit, so
@@ -421,44 +422,47 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    {
+      // ---------------- MMA issuer: the whole warp runs the loop converged, so
+      // descriptors and addresses stay warp-uniform, and one elected lane issues
+      // (a lone issuing lane competes for issue slots and slows the MMAs)
       int stage = 0, buf = 0, cur = blockIdx.x, tslot = 0;
       uint32_t ph = 0, bph = 0, tph = 0;
       bool ok = true, any = false;
-      for (int t = consume_tile(cur, tslot, tph, ok, false); ok && t >= 0;
-           t = consume_tile(cur, tslot, tph, ok, false)) {
+      const bool leader = elect_one();
+      for (int t = consume_tile(cur, tslot, tph, ok, true); ok && t >= 0;
+           t = consume_tile(cur, tslot, tph, ok, true)) {
         const typename P::Tile tile = P::tile(p, *sched, t);
         const int nk = P::num_k(p, tile);
-        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, p.status));
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + buf * kAccCols;
         for (int k = 0; k < nk; ++k) {
-          if (!mbar_wait(&full[stage], ph, abort_flag, p.status) ||
-              (P::CONVERT && !mbar_wait(&ready[stage], ph, abort_flag, p.status))) {
-            ok = false;
-            break;
-          }
+          bool got = mbar_wait(&full[stage], ph, abort_flag, p.status) &&
+                     (!P::CONVERT || mbar_wait(&ready[stage], ph, abort_flag, p.status));
+          ok = __all_sync(0xffffffffu, got);
+          if (!ok) break;
           tc_fence_after();
+          if (leader) {
 #pragma unroll
-          for (int sub = 0; sub < KSubOf<P>::value; ++sub) {
-            const uint32_t sa =
-                smem_u32(stages + stage * STAGE) + sub * StageGeom<P::BN, P::NA>::kBytes;
-            const uint64_t bdesc = umma_desc_sw128(sa + P::NA * kATileBytes);
+            for (int sub = 0; sub < KSubOf<P>::value; ++sub) {
+              const uint32_t sa =
+                  smem_u32(stages + stage * STAGE) + sub * StageGeom<P::BN, P::NA>::kBytes;
+              const uint64_t bdesc = umma_desc_sw128(sa + P::NA * kATileBytes);
 #pragma unroll
-            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              for (int kk = 0; kk < kTileK / 16; ++kk) {
 #pragma unroll
-              for (int a = 0; a < P::NA; ++a) {
-                const uint64_t adesc = umma_desc_sw128(sa + a * kATileBytes);
-                umma_bf16(d0 + a * P::BN, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
-                          (k | kk | sub) != 0 ? 1u : 0u);
+                for (int a = 0; a < P::NA; ++a) {
+                  const uint64_t adesc = umma_desc_sw128(sa + a * kATileBytes);
+                  umma_bf16(d0 + a * P::BN, adesc + 2 * kk, bdesc + 2 * kk, kIdesc,
+                            (k | kk | sub) != 0 ? 1u : 0u);
+                }
               }
             }
+            umma_commit(&empty[stage]);
           }
-          umma_commit(&empty[stage]);
+          __syncwarp();
           any = true;
           if (++stage == P::STAGES) {
             stage = 0;
@@ -466,16 +470,18 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[buf]);
+        if (leader) umma_commit(&tfull[buf]);
+        __syncwarp();
         if (++buf == P::NBUF) {
           buf = 0;
           bph ^= 1u;
         }
       }
-      if (!ok && any) {  // wait for the tensor cores before the memory is released
+      if (!ok && any && leader) {  // wait for the tensor cores before the memory is released
         umma_commit(drain);
         mbar_drain_wait(drain, 0);
       }
+      __syncwarp();
     }
   } else if (P::CONVERT && warp >= 8) {
     // ---------------- converters: raw packed weights -> swizzled operand tile
