@@ -161,9 +161,14 @@ struct ExpertGemmWT {
   static constexpr int AST_FIT = (512 - NBUF * NA * BN) / (kWtTilesPerStep * 32);
   static constexpr int AST = AST_FIT > 4 ? 4 : AST_FIT;
   static constexpr int RAW_BYTES = kWtTilesPerStep * Fmt::kTileBytes;
+  // activation ring: up to 6 steps ahead (they come from L2 with a long
+  // latency), in at most half the shared memory
+  static constexpr int B_SLOT = KS * BN * kTileK * 2;
+  static constexpr int BS_FIT = (kSmemLimit / 2) / B_SLOT;
+  static constexpr int BS = BS_FIT > 6 ? 6 : BS_FIT < 2 ? 2 : BS_FIT;
   // raw ring: what shared memory holds beside the activation slots (at most 8 steps)
   static constexpr int RS_FIT =
-      (kSmemLimit - 2048 - (int)sizeof(TileSched) - AST * KS * BN * kTileK * 2) / RAW_BYTES;
+      (kSmemLimit - 2048 - (int)sizeof(TileSched) - BS * KS * BN * kTileK * 2) / RAW_BYTES;
   static constexpr int RS = RS_FIT > 8 ? 8 : RS_FIT;
   static_assert(AST >= 2 && RS >= 2, "pipeline depth");
   static constexpr bool DYNAMIC = true;

@@ -23,7 +23,8 @@
 //                   raw ring (RS steps), freed by the converters
 //   warp 3 lane 0 : activation producer: the step's KS activation tiles (BN
 //                   token rows x 64 k, 128-byte swizzle, the MMA's B operand)
-//                   into the B slot of stage s % AST, freed by the MMA's commit
+//                   into a B ring of BS steps, freed by the MMA's commits, so
+//                   the activations are fetched well before the step is due
 //   warp 1 lane 0 : MMA issuer: tcgen05.mma kind::f16 with A from tensor
 //                   memory; one wait and one commit per step
 //   warp 2        : tensor-memory allocation / release (all 512 columns)
@@ -40,7 +41,7 @@
 // lets its copies and MMAs drain, frees tensor memory and returns.
 //
 // A problem class P supplies:
-//   static constexpr int BN, NA, KS, NBUF, AST, RS, RAW_BYTES;   (RAW_BYTES: one step)
+//   static constexpr int BN, NA, KS, NBUF, AST, RS, BS, RAW_BYTES;   (RAW_BYTES: one step)
 //   static constexpr bool DYNAMIC, PDL_PRIMARY, PDL_SECONDARY;
 //   struct Params { ...; uint32_t *status; uint32_t *sched_counters; };
 //   struct Sched; struct Tile;
@@ -78,7 +79,7 @@ __host__ __device__ constexpr int wt_b_slot_bytes() {
 // the programmatic dependent launch an SM still running gate/up.
 template <class P>
 __host__ __device__ constexpr int wt_smem_bytes() {
-  constexpr int need = 1024 + P::AST * wt_b_slot_bytes<P>() + P::RS * P::RAW_BYTES + 1024 +
+  constexpr int need = 1024 + P::BS * wt_b_slot_bytes<P>() + P::RS * P::RAW_BYTES + 1024 +
                        (int)sizeof(typename P::Sched);
   constexpr int half = kSmemLimit / 2 + 1024;
   return need > half ? need : half;
@@ -87,7 +88,7 @@ __host__ __device__ constexpr int wt_smem_bytes() {
 template <class P>
 __global__ void __launch_bounds__(kWtThreads, 1)
     wt_gemm_kernel(const __grid_constant__ typename P::Params p) {
-  constexpr int NA = P::NA, BN = P::BN, KS = P::KS, RS = P::RS, AST = P::AST;
+  constexpr int NA = P::NA, BN = P::BN, KS = P::KS, RS = P::RS, AST = P::AST, BS = P::BS;
   constexpr int BSLOT = wt_b_slot_bytes<P>();
   constexpr uint32_t kAccCols = NA * BN;
   constexpr uint32_t kACol0 = P::NBUF * kAccCols;
@@ -99,19 +100,20 @@ __global__ void __launch_bounds__(kWtThreads, 1)
   static_assert(kACol0 + AST * kStageCols <= kTmemCols, "tensor memory overflow");
   static_assert(BSLOT % 1024 == 0 && P::RAW_BYTES % 128 == 0, "slot alignment");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "invalid MMA N");
-  static_assert(AST >= 2 && RS >= 2, "pipeline depth");
+  static_assert(AST >= 2 && RS >= 2 && BS >= 2, "pipeline depth");
   constexpr uint32_t kConvWarpsPerStep = kWtConvWarps;  // every group takes part in every step
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *bslots = smem_raw + pad;
-  uint8_t *raws = bslots + AST * BSLOT;
+  uint8_t *raws = bslots + BS * BSLOT;
   uint8_t *bar_area = raws + RS * P::RAW_BYTES;
   uint64_t *raw_full = reinterpret_cast<uint64_t *>(bar_area);
   uint64_t *raw_empty = raw_full + RS;
   uint64_t *b_full = raw_empty + RS;
-  uint64_t *a_full = b_full + AST;   // A stage written and its B tiles landed
-  uint64_t *a_empty = a_full + AST;  // A stage and B slot free (the MMA's commit)
+  uint64_t *b_empty = b_full + BS;   // B slot free (the MMA's commit)
+  uint64_t *a_full = b_empty + BS;   // A stage written and its step's B tiles landed
+  uint64_t *a_empty = a_full + AST;  // A stage free (the MMA's commit)
   uint64_t *tfull = a_empty + AST;
   uint64_t *tempty = tfull + P::NBUF;
   uint64_t *drain = tempty + P::NBUF;
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tr_empty + kTileRing);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *tring = abort_flag + 1;
-  static_assert((2 * RS + 3 * AST + 2 * P::NBUF + 1 + 2 * kTileRing) * 8 + 8 + 4 * kTileRing <= 1024,
+  static_assert((2 * RS + 2 * BS + 2 * AST + 2 * P::NBUF + 1 + 2 * kTileRing) * 8 + 8 + 4 * kTileRing <= 1024,
                 "barrier area");
   typename P::Sched *sched = reinterpret_cast<typename P::Sched *>(bar_area + 1024);
 
@@ -132,8 +134,11 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], kConvWarpsPerStep);
     }
-    for (int s = 0; s < AST; ++s) {
+    for (int s = 0; s < BS; ++s) {
       mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < AST; ++s) {
       mbar_init(&a_full[s], kConvWarpsPerStep);
       mbar_init(&a_empty[s], 1);
     }
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     if (lane == 0) {
       // ---------------- activation producer (a down tile's h rows are read only
       // once tile_ready says its expert's gate/up tiles have published them)
-      int as = 0, cur = blockIdx.x, tslot = 0;
+      int bs = 0, cur = blockIdx.x, tslot = 0;
       uint32_t ph = 0, issued = 0, par = 0, tph = 0;
       bool ok = true;
       for (int t = consume_tile(cur, tslot, tph, ok, false); ok && t >= 0;
@@ -258,22 +263,22 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         const int ns = P::num_steps(p, tile);
         const uint32_t tx = P::b_tx_bytes(p, tile);
         for (int s = 0; s < ns; ++s) {
-          if (!mbar_wait(&a_empty[as], ph ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait(&b_empty[bs], ph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&b_full[as], tx);
-          P::load_b(p, tile, s, bslots + as * BSLOT, &b_full[as]);
-          issued |= 1u << as;
-          par = (par & ~(1u << as)) | (ph << as);
-          if (++as == AST) {
-            as = 0;
+          mbar_arrive_expect_tx(&b_full[bs], tx);
+          P::load_b(p, tile, s, bslots + bs * BSLOT, &b_full[bs]);
+          issued |= 1u << bs;
+          par = (par & ~(1u << bs)) | (ph << bs);
+          if (++bs == BS) {
+            bs = 0;
             ph ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < AST; ++s)
+        for (int s = 0; s < BS; ++s)
           if (issued & (1u << s)) mbar_drain_wait(&b_full[s], (par >> s) & 1u);
       }
     }
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       // ---------------- MMA issuer: the whole warp runs the loop converged,
       // so descriptors and addresses stay warp-uniform; one elected lane
       // issues.  One wait (a_full covers the B tiles too) and one commit per step.
-      int as = 0, buf = 0, cur = blockIdx.x, tslot = 0;
+      int as = 0, bs = 0, buf = 0, cur = blockIdx.x, tslot = 0;
       uint32_t aph = 0, bph = 0, tph = 0;
       bool ok = true, any = false;
       const uint32_t b0 = smem_u32(bslots);
@@ -299,17 +304,20 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         // MMAs, not right after step s: a barrier wait that follows a commit
         // at once stalls until the tensor core has drained, and it would then
         // sit idle while the next step is waited for and issued.
-        int prev = -1;  // stage whose commit is still due
+        int prev = -1, prevb = -1;  // stage and B slot whose commit is still due
         for (int s = 0; s < ns; ++s) {
           ok = __all_sync(0xffffffffu, mbar_wait(&a_full[as], aph, abort_flag, p.status));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t bst = b0 + as * BSLOT;
+          const uint32_t bst = b0 + bs * BSLOT;
           const uint32_t acol = tmem_base + kACol0 + as * kStageCols;
           if (leader) {
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-              if (j == KS / 2 && prev >= 0) umma_commit(&a_empty[prev]);
+              if (j == KS / 2 && prev >= 0) {
+                umma_commit(&a_empty[prev]);
+                umma_commit(&b_empty[prevb]);
+              }
               const uint64_t bdesc = umma_desc_sw128(bst + j * (BN * kTileK * 2));
 #pragma unroll
               for (int kk = 0; kk < kTileK / 16; ++kk) {
@@ -322,13 +330,18 @@ __global__ void __launch_bounds__(kWtThreads, 1)
           }
           __syncwarp();
           prev = as;
+          prevb = bs;
           any = true;
           if (++as == AST) {
             as = 0;
             aph ^= 1u;
           }
+          if (++bs == BS) bs = 0;
         }
-        if (leader && prev >= 0) umma_commit(&a_empty[prev]);
+        if (leader && prev >= 0) {
+          umma_commit(&a_empty[prev]);
+          umma_commit(&b_empty[prevb]);
+        }
         __syncwarp();
         if (!ok) break;
         if (leader) umma_commit(&tfull[buf]);
@@ -351,8 +364,8 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     const int row = q * 32 + lane;
     const int j = g / NA, a = g % NA;  // slice of the step, matrix
     const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + kACol0 + g * 32;
-    int rs = 0, as = 0, cur = blockIdx.x, tslot = 0;
-    uint32_t rph = 0, aph = 0, tph = 0;
+    int rs = 0, as = 0, bs = 0, cur = blockIdx.x, tslot = 0;
+    uint32_t rph = 0, aph = 0, bph2 = 0, tph = 0;
     bool ok = true;
     for (int t = consume_tile(cur, tslot, tph, ok, true); ok && t >= 0;
          t = consume_tile(cur, tslot, tph, ok, true)) {
@@ -373,12 +386,16 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         if (lane == 0) mbar_arrive(&raw_empty[rs]);  // the packed bytes are in registers
         tmem_st32(tq + as * kStageCols, v);
         tmem_wait_st();
-        // the stage is complete for the MMA once its B tiles have landed too
-        got = mbar_wait(&b_full[as], aph, abort_flag, p.status);
-        got = __all_sync(0xffffffffu, got);
-        if (!got) {
-          ok = false;
-          break;
+        // the stage is complete for the MMA once its B tiles have landed too:
+        // one warp checks (the stage completes only with every warp's arrival,
+        // so the MMA thread's wait on it covers the B tiles)
+        if (warp == 8) {
+          got = mbar_wait(&b_full[bs], bph2, abort_flag, p.status);
+          got = __all_sync(0xffffffffu, got);
+          if (!got) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -390,6 +407,10 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         if (++as == AST) {
           as = 0;
           aph ^= 1u;
+        }
+        if (++bs == BS) {
+          bs = 0;
+          bph2 ^= 1u;
         }
       }
     }
