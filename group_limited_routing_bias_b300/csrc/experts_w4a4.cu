@@ -17,7 +17,8 @@
 //
 // One CTA per SM, persistent; 640 threads:
 //   warp 0 lane 0 : TMA producer (codes with the 128-byte swizzle, scales plain)
-//   warp 1 lane 0 : MMA issuer: copies each stage's scales to tensor memory
+//   warp 1        : MMA issuer (the warp converged, one elected lane issuing):
+//                   copies each stage's scales to tensor memory
 //                   (tcgen05.cp) and issues the four K=64 MMAs of the stage
 //   warps 2, 3    : scale arrangers, alternate K slices: rearrange the stage's
 //                   scale bytes in shared memory into the 32 x 16-byte blocks
@@ -237,42 +238,44 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer: scale copies to tensor memory, then the MMAs
+    {
+      // ---------------- MMA issuer: scale copies to tensor memory, then the
+      // MMAs; the whole warp runs the loop converged and one elected lane issues
       constexpr uint32_t kIdesc = w4_idesc(kW4M, kW4N);
       int stage = 0;
       uint32_t ph = 0, bph = 0;
       bool ok = true, any = false;
+      const bool leader = elect_one();
       for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-        if (!mbar_wait(tempty, bph ^ 1u, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(tempty, bph ^ 1u, abort_flag, p.status));
+        if (!ok) break;
         tc_fence_after();
         for (int k = 0; k < p.ksteps; ++k) {
-          if (!mbar_wait(&full[stage], ph, abort_flag, p.status) ||
-              !mbar_wait(&sfready[stage], ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+          const bool got = mbar_wait(&full[stage], ph, abort_flag, p.status) &&
+                           mbar_wait(&sfready[stage], ph, abort_flag, p.status);
+          ok = __all_sync(0xffffffffu, got);
+          if (!ok) break;
           tc_fence_after();
-          uint8_t *st = stages + stage * kW4Stage;
-          const uint8_t *sfa = st + kW4ABytes + kW4BBytes;
-          const uint8_t *sfb = sfa + kW4SfABytes;
-          const uint32_t sf_t = tmem_base + kW4SfCol0 + stage * kW4SfStride;
+          if (leader) {
+            uint8_t *st = stages + stage * kW4Stage;
+            const uint8_t *sfa = st + kW4ABytes + kW4BBytes;
+            const uint8_t *sfb = sfa + kW4SfABytes;
+            const uint32_t sf_t = tmem_base + kW4SfCol0 + stage * kW4SfStride;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tmem_cp_sf(sf_t + 4 * j, sf_desc(smem_u32(sfa + j * 512)));
-            tmem_cp_sf(sf_t + 16 + 8 * j, sf_desc(smem_u32(sfb + (2 * j) * 512)));
-            tmem_cp_sf(sf_t + 16 + 8 * j + 4, sf_desc(smem_u32(sfb + (2 * j + 1) * 512)));
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_sf(sf_t + 4 * j, sf_desc(smem_u32(sfa + j * 512)));
+              tmem_cp_sf(sf_t + 16 + 8 * j, sf_desc(smem_u32(sfb + (2 * j) * 512)));
+              tmem_cp_sf(sf_t + 16 + 8 * j + 4, sf_desc(smem_u32(sfb + (2 * j + 1) * 512)));
+            }
+            const uint64_t adesc = umma_desc_sw128(smem_u32(st));
+            const uint64_t bdesc = umma_desc_sw128(smem_u32(st + kW4ABytes));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              umma_fp4(tmem_base, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_t + 4 * j,
+                       sf_t + 16 + 8 * j, (k | j) != 0 ? 1u : 0u);
+            umma_commit(&empty[stage]);
           }
-          const uint64_t adesc = umma_desc_sw128(smem_u32(st));
-          const uint64_t bdesc = umma_desc_sw128(smem_u32(st + kW4ABytes));
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            umma_fp4(tmem_base, adesc + 2 * j, bdesc + 2 * j, kIdesc, sf_t + 4 * j,
-                     sf_t + 16 + 8 * j, (k | j) != 0 ? 1u : 0u);
-          umma_commit(&empty[stage]);
+          __syncwarp();
           any = true;
           if (++stage == kW4Stages) {
             stage = 0;
@@ -280,13 +283,15 @@ __global__ void __launch_bounds__(kW4Threads, 1) w4a4_gemm_kernel(const __grid_c
           }
         }
         if (!ok) break;
-        umma_commit(tfull);
+        if (leader) umma_commit(tfull);
+        __syncwarp();
         bph ^= 1u;
       }
-      if (!ok && any) {  // wait for the tensor cores before the memory is released
+      if (!ok && any && leader) {  // wait for the tensor cores before the memory is released
         umma_commit(drain);
         mbar_drain_wait(drain, 0);
       }
+      __syncwarp();
     }
   } else if (warp == 2 || warp == 3) {
     // ---------------- scale arrangers: warp 2 takes the even K slices of the

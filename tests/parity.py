@@ -225,3 +225,27 @@ def sample_tokens(sample, idx, E: int):
         assert sample == "stratified"
         return stratified_tokens(idx, E, seed=T)
     return np.asarray(sample)
+
+
+def row_errors(y_gpu, y_ref):
+    """Per token row: (max|err| / max|ref|, ||err|| / ||ref||).  For batches
+    whose rows differ in scale by many orders of magnitude, where the norms
+    over the whole batch would only see the largest rows."""
+    a = np.asarray(y_gpu, np.float64)
+    b = np.asarray(y_ref, np.float64)
+    err = np.abs(a - b)
+    ref_max = np.abs(b).max(axis=1)
+    return (err.max(axis=1) / ref_max,
+            np.linalg.norm(a - b, axis=1) / np.linalg.norm(b, axis=1))
+
+
+def scale_rows(x: "torch.Tensor", big: float = 1e5, tiny: float = 1e-6, n: int = 4):
+    """x bf16 [T, H] with rows 0..n-1 scaled so their largest |value| is about
+    `big`, rows n..2n-1 scaled to about `tiny` (values far outside f16's
+    range, and deep in its subnormals); the rest unchanged."""
+    import torch
+    y = x.float().clone()
+    for r in range(n):
+        y[r] *= big / y[r].abs().max()
+        y[n + r] *= tiny / y[n + r].abs().max()
+    return y.to(torch.bfloat16)

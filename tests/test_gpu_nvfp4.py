@@ -15,7 +15,7 @@ import torch
 import moe_inputs as mi
 import oracle
 from parity import (NVFP4_REL_FROB, compare_routing, output_errors, reference_routing,
-                    sample_tokens)
+                    row_errors, sample_tokens, scale_rows)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -102,6 +102,29 @@ def test_nvfp4_beam(lib, T, sample):
     """The four batch sizes of the NVFP4 workload; from T=1024 every touched
     expert's first row, last-tile boundary rows and last row are compared."""
     check(lib, Fp4Case(mi.CONFIGS["nvfp4"], T=T), sample)
+
+
+def test_nvfp4_bf16_activation_range(lib):
+    """The packed-weight path of decode-sized batches (weights dequantised into
+    tensor memory, bf16 activations): token rows with |x| up to 1e5 and rows
+    of about 1e-6, every row within the bf16 bars relative to its own scale."""
+    case = Fp4Case(mi.CONFIGS["nvfp4"], T=64)
+    case.x_h = scale_rows(case.x_h)
+    case.x = case.x_h.to(DEV)
+    c = case.cfg
+    y, idx, w = forward(lib, case)
+    orc = oracle.route(mi.bf16_bits(case.x_h), case.wr_h.numpy(), case.b_h.numpy(), c.n_group,
+                       c.topk_group, c.top_k, c.routed_scale, details=True)
+    rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
+    assert rep.ok, (rep, rep.mismatch_info)
+    ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
+    tokens = np.arange(16)
+    y_ref = oracle.experts_forward(mi.bf16_bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
+    yg = y.double().cpu().numpy()[tokens]
+    assert np.isfinite(yg).all()
+    mx, fr = row_errors(yg, y_ref)
+    print(f"\n[nvfp4 T=64] rows |x|~1e5: rel-Frob {fr[:4]}; |x|~1e-6: {fr[4:8]}")
+    assert (mx <= 2e-2).all() and (fr <= 5e-3).all(), (mx, fr)
 
 
 @pytest.mark.parametrize("T", [5, 64, 2048])

@@ -17,7 +17,8 @@ import torch
 import moe_inputs as mi
 import oracle
 from parity import (LOGIT_ATOL, W_RTOL, compare_routing, output_errors, reference_routing,
-                    stratified_tokens)
+                    row_errors, stratified_tokens)
+from parity import scale_rows as mi_scale_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -331,6 +332,29 @@ def test_stages_match_forward(lib, T):
     got = yp[so.ravel()].reshape(c.T, c.top_k, c.H)
     err = output_errors(got, rows_ref)
     assert err.ok(), err
+
+
+@pytest.mark.parametrize("name,T", [("decode", 64), ("tiny", 2048)])
+def test_forward_bf16_activation_range(lib, name, T):
+    """Token rows with |x| up to 1e5 and rows of about 1e-6 keep bf16's range
+    through the whole block (h of the large rows reaches ~1e10): every row
+    within the bf16 bars relative to its own scale.  decode T=64 runs the
+    weights-on-M GEMMs, tiny T=2048 the token-major ones."""
+    case = Case(mi.CONFIGS[name], T=T)
+    case.x_h = mi_scale_rows(case.x_h)
+    case.x = case.x_h.to(DEV)
+    c = case.cfg
+    y, idx, w = forward(lib, case)
+    orc = case.oracle_route()
+    rep = check_routing(case, orc, idx, w, max_flag_frac=0.2)
+    ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
+    tokens = np.arange(16)
+    y_ref = oracle.experts_forward(bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
+    assert np.isfinite(y[tokens]).all()
+    mx, fr = row_errors(y[tokens], y_ref)
+    print(f"\n[{c.name} T={c.T}] rows |x|~1e5: rel-Frob {fr[:4]}; |x|~1e-6: {fr[4:8]}; "
+          f"max |y| {np.abs(y_ref[:4]).max():.3g} / {np.abs(y_ref[4:8]).max():.3g}")
+    assert (mx <= 2e-2).all() and (fr <= 5e-3).all(), (mx, fr)
 
 
 def test_zero_down_weights_give_zero(lib):
