@@ -270,9 +270,12 @@ moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts, 
     return launch_experts_w4a4(*dims, *experts, xq, xs, expert_offsets, row_src, topk_w, y_partial,
                                at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status_word(ws), s);
   }
-  if (experts->dtype != MOE_W_BF16 && packed_wt_applies(*dims))
+  if (experts->dtype != MOE_W_BF16 && packed_wt_applies(*dims)) {
+    const PackedWtScratch scr{at<void>(ws, L.x16), at<void>(ws, L.h), at<float>(ws, L.xscale),
+                              at<uint32_t>(ws, L.hmax), at<float>(ws, L.hscale)};
     return launch_experts_packed_wt(*dims, *experts, x_perm, expert_offsets, row_src, topk_w,
-                                    y_partial, at<__nv_bfloat16>(ws, L.h), status_word(ws), s);
+                                    y_partial, scr, status_word(ws), s);
+  }
   if (experts->dtype != MOE_W_BF16) {
     void *x16 = at<void>(ws, L.x16);
     const size_t n = (size_t)dims->T * dims->top_k * dims->H;
@@ -309,7 +312,8 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   const bool a4 = experts->dtype == MOE_W_NVFP4_A4;
   const bool packed = experts->dtype != MOE_W_BF16 && !a4;
   // packed weights: small and mid-size batches dequantise into tensor memory
-  // with bf16 activations; large ones run the token-major GEMMs on f16 ones
+  // (activations as f16 with a power-of-two scale per row); large ones run the
+  // token-major GEMMs on plain f16 activations
   const bool packed_wt = packed && packed_wt_applies(d);
   const bool fp4 = packed && !packed_wt;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -338,9 +342,13 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
       return st;
     st = launch_experts_w4a4(d, *experts, xq, xs, offsets, row_src, w, y_partial,
                              at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status, s);
-  } else if (packed_wt)
-    st = launch_experts_packed_wt(d, *experts, x_perm, offsets, row_src, w, y_partial,
-                                  at<__nv_bfloat16>(ws, L.h), status, s);
+  } else if (packed_wt) {
+    // x_perm is scaled to f16 in place
+    const PackedWtScratch scr{x_perm, at<void>(ws, L.h), at<float>(ws, L.xscale),
+                              at<uint32_t>(ws, L.hmax), at<float>(ws, L.hscale)};
+    st = launch_experts_packed_wt(d, *experts, x_perm, offsets, row_src, w, y_partial, scr, status,
+                                  s);
+  }
   else if (fp4)
     st = launch_experts_fp4(d, *experts, x_perm, offsets, row_src, w, y_partial, at<void>(ws, L.h),
                             status, s);

@@ -7,18 +7,31 @@
 //   h = silu(X_e . W_gate[e]^T) * (X_e . W_up[e]^T)
 //   y_partial = topk_w * (h . W_down[e]^T)
 //
-// Operands are bf16 on both sides, so the activations keep bf16's range: a
-// weight e2m1 * e4m3 (at most six significant bits, in [2^-10, 2688]) or an
-// e4m3 code is exact in bf16.  A converter thread dequantises one weight row
-// of a 64-wide K slice: e2m1 (or e4m3) pairs to f16 pairs by the hardware
-// conversion, times the f16 block scale (exact), widened to fp32 and packed to
-// bf16 pairs (exact).  The NVFP4 global scale and the FP8 row scales multiply
-// the fp32 accumulator in the epilogue.  x_perm and h stay bf16.
+// Operands are f16 on both sides.  A weight e2m1 * e4m3 (at most six
+// significant bits, in [2^-10, 2688]) or an e4m3 code is exact in f16: a
+// converter thread dequantises one weight row of a 64-wide K slice, e2m1 (or
+// e4m3) pairs to f16 pairs by the hardware conversion, times the f16 block
+// scale (exact).  The activations keep bf16's range through one power-of-two
+// scale per token row: each row of x_perm, and each row of h once its expert's
+// gate/up tiles are all done, is multiplied by the power of two that puts its
+// largest magnitude in [2^14, 2^15) and stored as f16.  Every bf16 value of
+// the row is then exact in f16, except values below 2^-28 of the row's
+// largest, which become f16 subnormals (absolute error at most 2^-39 of it).
+// The MMAs see the scaled rows, so each accumulator column carries its row's
+// factor; the epilogue multiplies it back out (exactly, a power of two)
+// together with the NVFP4 global or the FP8 row scale.  The products are
+// exact and the tensor cores' accumulation is invariant under such a scaling,
+// so the results are those of bf16 operands.
 //
-// Tiles, schedule and the gate/up -> down hand-off are those of the bf16
-// weights-on-M GEMMs in experts.cu: tiles are taken from a global counter,
-// the down GEMM is a programmatic dependent of gate/up and each down tile
-// waits (bounded) until its expert's h rows are published.
+// Tiles are taken from a global counter as in the bf16 weights-on-M GEMMs of
+// experts.cu.  The gate/up epilogue writes bf16 h and gathers each row's
+// largest |h|; a small kernel running beside gate/up (a programmatic
+// dependent of it) rescales an expert's rows of h to f16 in place as soon as
+// the expert's gate/up tiles are done, and publishes them; the down GEMM (a
+// programmatic dependent of that kernel) starts as gate/up's CTAs leave
+// their SMs and each down tile waits (bounded) for its expert's rows.
+#include <cuda_fp16.h>
+
 #include "moe_internal.cuh"
 #include "sched.cuh"
 #include "tc_gemm_wtmem.cuh"
@@ -27,23 +40,10 @@ namespace beam {
 
 namespace {
 
-// Two f16 values -> the same two values as bf16 (exact for every value
-// produced here: at most 11 significant bits are never needed, all are normal
-// or zero in bf16's range).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-  float lo, hi;
-  asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h));
-  uint32_t o;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(hi), "f"(lo));
-  return o;
-}
-
 // One NVFP4 weight row of a 64-wide K slice: 32 code bytes (even k in the low
-// nibble) and the four e4m3 scales of its 16-k blocks -> 32 bf16 pairs.
-__device__ __forceinline__ void nvfp4_row_bf16(uint4 c0, uint4 c1, uint32_t scales,
-                                               uint32_t (&out)[32]) {
+// nibble) and the four e4m3 scales of its 16-k blocks -> 32 f16 pairs.
+__device__ __forceinline__ void nvfp4_row_f16(uint4 c0, uint4 c1, uint32_t scales,
+                                              uint32_t (&out)[32]) {
   uint32_t s16[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
@@ -63,30 +63,146 @@ __device__ __forceinline__ void nvfp4_row_bf16(uint4 c0, uint4 c1, uint32_t scal
         : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
         : "r"(w[i]));
     const uint32_t s = s16[i >> 1];
-    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h0) : "r"(s));
-    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h1) : "r"(s));
-    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h2) : "r"(s));
-    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h3) : "r"(s));
-    out[4 * i + 0] = f16x2_to_bf16x2(h0);
-    out[4 * i + 1] = f16x2_to_bf16x2(h1);
-    out[4 * i + 2] = f16x2_to_bf16x2(h2);
-    out[4 * i + 3] = f16x2_to_bf16x2(h3);
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 0]) : "r"(h0), "r"(s));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 1]) : "r"(h1), "r"(s));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 2]) : "r"(h2), "r"(s));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 3]) : "r"(h3), "r"(s));
   }
 }
 
-// One FP8 weight row of a 64-wide K slice: 64 e4m3 codes -> 32 bf16 pairs.
-__device__ __forceinline__ void fp8_row_bf16(const uint8_t *codes, uint32_t (&out)[32]) {
+// One FP8 weight row of a 64-wide K slice: 64 e4m3 codes -> 32 f16 pairs.
+__device__ __forceinline__ void fp8_row_f16(const uint8_t *codes, uint32_t (&out)[32]) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const uint4 q = *reinterpret_cast<const uint4 *>(codes + 16 * v);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint32_t lo, hi;
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((uint16_t)(w[i] & 0xFFFFu)));
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((uint16_t)(w[i] >> 16)));
-      out[8 * v + 2 * i] = f16x2_to_bf16x2(lo);
-      out[8 * v + 2 * i + 1] = f16x2_to_bf16x2(hi);
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out[8 * v + 2 * i]) : "h"((uint16_t)(w[i] & 0xFFFFu)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out[8 * v + 2 * i + 1]) : "h"((uint16_t)(w[i] >> 16)));
+    }
+  }
+}
+
+// The power of two that brings a row whose largest magnitude has the fp32
+// exponent field e32 into [2^14, 2^15): 2^(141 - e32), at most 2^127 (rows of
+// zeros or of values below 2^-113).  Returns its exponent.
+__device__ __forceinline__ int row_scale_exp(uint32_t e32) {
+  return min(127, 141 - (int)e32);
+}
+
+// bf16 pairs -> the same values times s (a power of two) as f16 pairs (exact
+// but for the subnormal tail); 8 values per 16-byte vector.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float s) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16) * s;
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * s;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(hi), "f"(lo));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Rows of x_perm (bf16 [rows, K]) -> f16 rows scaled by a power of two each
+// (see above); rscale[r] receives the inverse factor and hmax[r] is cleared
+// for the gate/up epilogue's maxima.  dst may equal src (each value is read
+// and written by one lane).  One warp per row.  Launched as an ordinary
+// kernel; the gate/up GEMM is its programmatic dependent.
+__global__ void __launch_bounds__(256) rows_f16_scaled_kernel(const __nv_bfloat16 *src,
+                                                              __half *dst, int rows, int K,
+                                                              float *rscale, uint32_t *hmax) {
+  // the gate/up GEMM may start streaming weights; it reads x16 only after
+  // this kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)r * K);
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst + (size_t)r * K);
+  const int n4 = K / 8;
+  uint32_t m = 0;  // largest |bf16| bit pattern of the lane's values (per half)
+#pragma unroll 8
+  for (int i = lane; i < n4; i += 32) {
+    const uint4 v = s4[i];
+    m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                             __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+  m = __reduce_max_sync(0xffffffffu, m);
+  const int sx = row_scale_exp(m >> 7);  // bf16 and fp32 share the exponent field
+  const float sc = ldexpf(1.0f, sx);
+#pragma unroll 8
+  for (int i = lane; i < n4; i += 32) d4[i] = bf16x8_to_f16x8_scaled(s4[i], sc);
+  if (lane == 0) {
+    rscale[r] = ldexpf(1.0f, -sx);
+    hmax[r] = 0u;
+  }
+}
+
+// Rows of h (bf16 [Tk, K], in place) -> f16 scaled by the power of two that
+// their largest magnitude hmax[r] (fp32 bits, gathered by the gate/up
+// epilogue) asks for; hscale[r] receives the inverse factor.  A programmatic
+// dependent of the gate/up GEMM that runs beside it: CTA b takes experts b,
+// b + grid, ...; for each it waits (bounded) until every gate/up epilogue
+// warp of the expert has counted (4 per feature tile and token tile of bn
+// rows), rescales the expert's rows (one warp per row, four warps) and counts
+// once more, which publishes them to the down GEMM's TMA reads.
+__global__ void __launch_bounds__(128) h_rows_f16_scaled_kernel(
+    __nv_bfloat16 *h, const int32_t *offsets, int E, int K, int bn, int up_mt,
+    const uint32_t *hmax, float *hscale, uint32_t *expert_done, uint32_t *status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ int ok;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n4 = K / 8;
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int r0 = __ldg(offsets + e), r1 = __ldg(offsets + e + 1);
+    if (r1 == r0) continue;
+    if (threadIdx.x == 0) {
+      const uint32_t need = 4u * (uint32_t)up_mt * (uint32_t)((r1 - r0 + bn - 1) / bn);
+      ok = 1;
+      if (ld_acquire_gpu(expert_done + e) < need) {
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_gpu(expert_done + e) < need) {
+          if (ld_acquire_gpu(status) & (uint32_t)MOE_DEV_TIMEOUT) {
+            ok = 0;  // a GEMM gave up: so does this
+            break;
+          }
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, (uint32_t)MOE_DEV_TIMEOUT);
+            ok = 0;
+            break;
+          }
+          __nanosleep(200);
+        }
+      }
+    }
+    __syncthreads();
+    if (!ok) return;
+    for (int r = r0 + warp; r < r1; r += 4) {
+      const int sx = row_scale_exp(__ldcg(hmax + r) >> 23);
+      const float sc = ldexpf(1.0f, sx);
+      uint4 *row = reinterpret_cast<uint4 *>(h + (size_t)r * K);
+      for (int i0 = 0; i0 < n4; i0 += 32 * 8) {  // eight 16-byte loads in flight per lane
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * 32 + lane;
+          if (i < n4) v[u] = __ldcg(row + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * 32 + lane;
+          if (i < n4) row[i] = bf16x8_to_f16x8_scaled(v[u], sc);
+        }
+      }
+      if (lane == 0) hscale[r] = ldexpf(1.0f, -sx);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(expert_done + e, 1u);
     }
   }
 }
@@ -100,7 +216,7 @@ struct WtNvfp4 {
   __device__ static void convert(const uint8_t *t, int k, int r, uint32_t (&out)[32]) {
     const uint4 *c = reinterpret_cast<const uint4 *>(t + r * 32);
     const uint32_t sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 16 + (k & 3) * 4);
-    nvfp4_row_bf16(c[0], c[1], sc, out);
+    nvfp4_row_f16(c[0], c[1], sc, out);
   }
 };
 // Tiled NVFP4 (moe_pack_nvfp4): codes [128][32 B], then scales [128][4 B].
@@ -110,7 +226,7 @@ struct WtNvfp4Tiled {
   __device__ static void convert(const uint8_t *t, int, int r, uint32_t (&out)[32]) {
     const uint4 *c = reinterpret_cast<const uint4 *>(t + r * 32);
     const uint32_t sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 4);
-    nvfp4_row_bf16(c[0], c[1], sc, out);
+    nvfp4_row_f16(c[0], c[1], sc, out);
   }
 };
 // FP8, row-major (TMA box) or tiled (moe_pack_fp8): codes [128][64 B].
@@ -118,7 +234,7 @@ struct WtFp8 {
   static constexpr bool kTiled = false, kPerRowScale = true;
   static constexpr int kTileBytes = 8192;
   __device__ static void convert(const uint8_t *t, int, int r, uint32_t (&out)[32]) {
-    fp8_row_bf16(t + r * 64, out);
+    fp8_row_f16(t + r * 64, out);
   }
 };
 struct WtFp8Tiled : WtFp8 {
@@ -126,7 +242,7 @@ struct WtFp8Tiled : WtFp8 {
 };
 
 struct WtParams {
-  CUtensorMap tmap_b;    // token rows [Tk, K] bf16 (x_perm or h), box {64, BN}
+  CUtensorMap tmap_b;    // scaled f16 token rows [Tk, K] (x16 or h), box {64, BN}
   CUtensorMap tmap_bh;   // the same rows, box {64, BN / 2}
   CUtensorMap tmap_q0;   // row-major codes of W_gate or W_down
   CUtensorMap tmap_q1;   // row-major codes of W_up
@@ -140,11 +256,13 @@ struct WtParams {
   const int32_t *row_src;
   const float *topk_w;
   __nv_bfloat16 *out;  // h [Tk, I] or y_partial [Tk, H]
+  const float *bscale;  // [Tk] inverse row factor of the B operand (x16 or h)
+  uint32_t *hmax;       // [Tk] gate/up: largest |h| of each row (fp32 bits)
   int E, out_cols, w_rows, ksteps, mt;
   uint32_t *status;
   uint32_t *sched_counters;  // dynamic tile schedule (workspace header)
   uint32_t *expert_done;     // [E] gate/up epilogue warps done per expert (workspace header)
-  int up_mt;                 // gate/up feature tiles per token tile (down: readiness target)
+  int up_mt;                 // gate/up feature tiles per token tile
 };
 
 __device__ __forceinline__ float wt_scale(const float *g, int scale_rows, int e, int n) {
@@ -172,8 +290,12 @@ struct ExpertGemmWT {
   static constexpr int RS = RS_FIT > 8 ? 8 : RS_FIT;
   static_assert(AST >= 2 && RS >= 2, "pipeline depth");
   static constexpr bool DYNAMIC = true;
-  static constexpr bool PDL_PRIMARY = GATEUP;
-  static constexpr bool PDL_SECONDARY = !GATEUP;
+  // every launch of the chain x16 rescaling -> gate/up -> h rescaling -> down
+  // is a programmatic dependent of the one before: gate/up reads x16 after
+  // waiting for its kernel to complete, down each expert's h once published
+  static constexpr bool PDL_PRIMARY = true;
+  static constexpr bool PDL_SECONDARY = true;
+  static constexpr bool PDL_WAIT_B = GATEUP;
 
   using Params = WtParams;
   using Sched = TileSched;
@@ -232,22 +354,23 @@ struct ExpertGemmWT {
                                      int j, int a, int row, uint32_t (&out)[32]) {
     Fmt::convert(raw + (j * NA + a) * Fmt::kTileBytes, s * KS + j, row, out);
   }
-  // gate/up: each epilogue warp publishes its 32 features of h for the tile
-  // (release: its stores before the count, for the down GEMM's TMA reads)
+  // gate/up: each epilogue warp counts its 32 features of h for the tile (its
+  // stores and row maxima before the count); the h rescaling kernel waits for
+  // the expert's count to complete
   __device__ static void tile_done(const Params &p, const Tile &t) {
     if constexpr (GATEUP) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
       __threadfence();
       atomicAdd(p.expert_done + t.e, 1u);
     }
   }
-  // down: wait until every gate/up tile of the expert (4 epilogue warps each)
-  // has been published, then order the TMA reads of h after that
+  // down: wait until the rescaling kernel has published the expert's f16 h
+  // rows (one count beyond the gate/up warps'), then order the TMA reads of h
+  // after that
   __device__ static bool tile_ready(const Params &p, const Tile &t, volatile int *abort) {
     if constexpr (GATEUP) {
       return true;
     } else {
-      const uint32_t need = 4u * (uint32_t)p.up_mt * (uint32_t)t.ntt;
+      const uint32_t need = 4u * (uint32_t)p.up_mt * (uint32_t)t.ntt + 1u;
       const uint32_t *cnt = p.expert_done + t.e;
       if (ld_acquire_gpu(cnt) < need) {
         const uint64_t t0 = global_timer_ns();
@@ -270,33 +393,63 @@ struct ExpertGemmWT {
     if constexpr (!GATEUP)
       for (int e = 0; e < p.E; ++e) p.expert_done[e] = 0;
   }
+  // Accumulator column n is token row row0 + n scaled by the row's factor:
+  // multiplied back by bscale first (exact), then by the weight scales.  Lane
+  // l loads the factors of rows row0 + l, row0 + 32 + l, ... once per tile;
+  // each column takes them from its lane with a shuffle.
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
+    constexpr int NG = BN / 32;  // 32-row groups of the tile
     const int f = t.m * kTileM + row;  // output feature of this thread
+    const int lane = row & 31;
     const float ga = wt_scale(p.g0, p.scale_rows, t.e, f);
     const float gb = GATEUP ? wt_scale(p.g1, p.scale_rows, t.e, f) : 0.f;
-    for (int c = 0; c < t.nrows; c += 16) {
-      uint32_t a[16];
-      tmem_ld16(taddr + c, a);
-      if (GATEUP) {
-        uint32_t u[16];
-        tmem_ld16(taddr + BN + c, u);
-        tmem_wait_ld();
+    float bs_l[NG], tw_l[NG];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c + j < t.nrows) {
-            const float gv = __uint_as_float(a[j]) * ga;
-            const float hv = gv / (1.0f + __expf(-gv)) * (__uint_as_float(u[j]) * gb);
-            p.out[(size_t)(t.row0 + c + j) * p.out_cols + f] = __float2bfloat16_rn(hv);
+    for (int i = 0; i < NG; ++i) {
+      const int n = i * 32 + lane;
+      bs_l[i] = tw_l[i] = 0.f;
+      if (n < t.nrows) {
+        const int r = t.row0 + n;
+        bs_l[i] = __ldcg(p.bscale + r);
+        if (!GATEUP) tw_l[i] = __ldg(p.topk_w + __ldg(p.row_src + r));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NG; ++i) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c = i * 32 + hf * 16;
+        if (c >= t.nrows) break;
+        uint32_t a[16];
+        tmem_ld16(taddr + c, a);
+        if (GATEUP) {
+          uint32_t u[16];
+          tmem_ld16(taddr + BN + c, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float bs = __shfl_sync(0xffffffffu, bs_l[i], hf * 16 + j);
+            uint32_t mag = 0;
+            if (c + j < t.nrows) {
+              const float gv = __uint_as_float(a[j]) * bs * ga;
+              const float hv = gv / (1.0f + __expf(-gv)) * (__uint_as_float(u[j]) * bs * gb);
+              const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+              p.out[(size_t)(t.row0 + c + j) * p.out_cols + f] = hb;
+              mag = __float_as_uint(fabsf(__bfloat162float(hb)));
+            }
+            // the row's largest |h| over this warp's 32 features, one atomic per row
+            mag = __reduce_max_sync(0xffffffffu, mag);
+            if (lane == j && c + j < t.nrows) atomicMax(p.hmax + t.row0 + c + j, mag);
           }
-        }
-      } else {
-        tmem_wait_ld();
+        } else {
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c + j < t.nrows) {
-            const int r = t.row0 + c + j;
-            const float w = __ldg(p.topk_w + __ldg(p.row_src + r)) * ga;
-            p.out[(size_t)r * p.out_cols + f] = __float2bfloat16_rn(__uint_as_float(a[j]) * w);
+          for (int j = 0; j < 16; ++j) {
+            const float bs = __shfl_sync(0xffffffffu, bs_l[i], hf * 16 + j);
+            const float w = __shfl_sync(0xffffffffu, tw_l[i], hf * 16 + j) * ga;
+            if (c + j < t.nrows)
+              p.out[(size_t)(t.row0 + c + j) * p.out_cols + f] =
+                  __float2bfloat16_rn(__uint_as_float(a[j]) * bs * w);
           }
         }
       }
@@ -321,7 +474,7 @@ moe_status launch_wt(const WtParams &prm, int grid, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = P::PDL_SECONDARY ? 1 : 0;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, wt_gemm_kernel<P>, prm) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -352,15 +505,22 @@ bool wt_weights(WtParams &prm, const void *w0, const void *s0, const void *w1, c
 template <class Fmt, int BN>
 moe_status launch_wt_bn(const moe_dims &d, const moe_experts &ex, const void *x_perm,
                         const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                        void *y_partial, __nv_bfloat16 *h, uint32_t *status, cudaStream_t stream) {
+                        void *y_partial, const PackedWtScratch &scr, uint32_t *status,
+                        cudaStream_t stream) {
   const long Tk = (long)d.T * d.top_k;
   const long max_tt = Tk / BN + std::min<long>(d.E, Tk);
   const int sms = device_sm_count();
+  __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(scr.h);
+  rows_f16_scaled_kernel<<<(unsigned)((Tk + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(x_perm), static_cast<__half *>(scr.x16), (int)Tk, d.H,
+      scr.xscale, scr.hmax);
+  if (cudaPeekAtLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  // the tensor maps only move 2-byte elements: the bf16 maps serve the f16 rows
   {
     WtParams prm{};
     const long rows = (long)d.E * d.I;
-    if (!make_tmap_bf16_2d(&prm.tmap_b, x_perm, d.H, Tk, BN) ||
-        !make_tmap_bf16_2d(&prm.tmap_bh, x_perm, d.H, Tk, BN / 2) ||
+    if (!make_tmap_bf16_2d(&prm.tmap_b, scr.x16, d.H, Tk, BN) ||
+        !make_tmap_bf16_2d(&prm.tmap_bh, scr.x16, d.H, Tk, BN / 2) ||
         !wt_weights<Fmt>(prm, ex.w_gate, ex.s_gate, ex.w_up, ex.s_up, d.H, rows))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_gate;
@@ -370,6 +530,8 @@ moe_status launch_wt_bn(const moe_dims &d, const moe_experts &ex, const void *x_
     prm.row_src = row_src;
     prm.topk_w = topk_w;
     prm.out = h;
+    prm.bscale = scr.xscale;
+    prm.hmax = scr.hmax;
     prm.E = d.E;
     prm.out_cols = d.I;
     prm.w_rows = d.I;
@@ -382,6 +544,25 @@ moe_status launch_wt_bn(const moe_dims &d, const moe_experts &ex, const void *x_
     const int grid = (int)std::max<long>(1, std::min<long>(sms, max_tt * prm.mt));
     const moe_status st = launch_wt<ExpertGemmWT<Fmt, BN, true>>(prm, grid, stream);
     if (st != MOE_OK) return st;
+  }
+  {
+    // h rows -> scaled f16 in place, expert by expert beside gate/up: one
+    // CTA of 128 threads per SM fits beside a gate/up or a down CTA (registers)
+    const int grid = std::max(1, std::min(sms, d.E));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, h_rows_f16_scaled_kernel, h, offsets, d.E, d.I, BN,
+                           d.I / kTileM, (const uint32_t *)scr.hmax, scr.hscale,
+                           status + kExpertDoneWord, status) != cudaSuccess ||
+        cudaPeekAtLastError() != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   {
     WtParams prm{};
@@ -397,6 +578,7 @@ moe_status launch_wt_bn(const moe_dims &d, const moe_experts &ex, const void *x_
     prm.row_src = row_src;
     prm.topk_w = topk_w;
     prm.out = static_cast<__nv_bfloat16 *>(y_partial);
+    prm.bscale = scr.hscale;
     prm.E = d.E;
     prm.out_cols = d.H;
     prm.w_rows = d.H;
@@ -414,11 +596,12 @@ moe_status launch_wt_bn(const moe_dims &d, const moe_experts &ex, const void *x_
 template <class Fmt>
 moe_status launch_wt_fmt(const moe_dims &d, const moe_experts &ex, const void *x_perm,
                          const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                         void *y_partial, __nv_bfloat16 *h, uint32_t *status, cudaStream_t stream) {
+                         void *y_partial, const PackedWtScratch &scr, uint32_t *status,
+                         cudaStream_t stream) {
   switch (expert_tile_rows(d)) {
-    case 32: return launch_wt_bn<Fmt, 32>(d, ex, x_perm, offsets, row_src, topk_w, y_partial, h, status, stream);
-    case 64: return launch_wt_bn<Fmt, 64>(d, ex, x_perm, offsets, row_src, topk_w, y_partial, h, status, stream);
-    default: return launch_wt_bn<Fmt, 128>(d, ex, x_perm, offsets, row_src, topk_w, y_partial, h, status, stream);
+    case 32: return launch_wt_bn<Fmt, 32>(d, ex, x_perm, offsets, row_src, topk_w, y_partial, scr, status, stream);
+    case 64: return launch_wt_bn<Fmt, 64>(d, ex, x_perm, offsets, row_src, topk_w, y_partial, scr, status, stream);
+    default: return launch_wt_bn<Fmt, 128>(d, ex, x_perm, offsets, row_src, topk_w, y_partial, scr, status, stream);
   }
 }
 
@@ -432,19 +615,20 @@ bool packed_wt_applies(const moe_dims &d) {
 
 moe_status launch_experts_packed_wt(const moe_dims &d, const moe_experts &ex, const void *x_perm,
                                     const int32_t *expert_offsets, const int32_t *row_src,
-                                    const float *topk_w, void *y_partial, __nv_bfloat16 *h,
-                                    uint32_t *status, cudaStream_t stream) {
+                                    const float *topk_w, void *y_partial,
+                                    const PackedWtScratch &scr, uint32_t *status,
+                                    cudaStream_t stream) {
   const bool tiled = ex.layout == MOE_LAYOUT_TILED;
   if (ex.dtype == MOE_W_FP8)
     return tiled ? launch_wt_fmt<WtFp8Tiled>(d, ex, x_perm, expert_offsets, row_src, topk_w,
-                                             y_partial, h, status, stream)
+                                             y_partial, scr, status, stream)
                  : launch_wt_fmt<WtFp8>(d, ex, x_perm, expert_offsets, row_src, topk_w, y_partial,
-                                        h, status, stream);
+                                        scr, status, stream);
   if (ex.dtype == MOE_W_NVFP4)
     return tiled ? launch_wt_fmt<WtNvfp4Tiled>(d, ex, x_perm, expert_offsets, row_src, topk_w,
-                                               y_partial, h, status, stream)
+                                               y_partial, scr, status, stream)
                  : launch_wt_fmt<WtNvfp4>(d, ex, x_perm, expert_offsets, row_src, topk_w,
-                                          y_partial, h, status, stream);
+                                          y_partial, scr, status, stream);
   return MOE_ERR_NOT_IMPLEMENTED;
 }
 

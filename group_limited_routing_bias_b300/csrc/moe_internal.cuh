@@ -75,7 +75,8 @@ struct WsLayout {
   size_t counts = 0, bases = 0;                     // permute
   size_t offsets = 0, slot_of = 0, row_src = 0, x_perm = 0;  // forward only
   size_t h = 0;                                     // experts
-  size_t x16 = 0;                                   // experts, NVFP4 only
+  size_t x16 = 0;                                   // experts, NVFP4 or FP8 only
+  size_t xscale = 0, hmax = 0, hscale = 0;          // experts and forward, NVFP4 or FP8 only
   size_t xq = 0, xs = 0, hq = 0, hs = 0;            // experts and forward, W4A4 only
   size_t y_partial = 0;                             // forward only
   size_t total = 0;
@@ -121,6 +122,11 @@ inline WsLayout ws_layout(const moe_dims &d, moe_op op, moe_wdtype wdtype = MOE_
     L.h = take(Tk * d.I * 2);
   }
   if (op == MOE_OP_EXPERTS && wdtype != MOE_W_BF16 && !a4) L.x16 = take(Tk * d.H * 2);
+  if ((op == MOE_OP_EXPERTS || fwd) && wdtype != MOE_W_BF16 && !a4) {
+    L.xscale = take(Tk * 4);
+    L.hmax = take(Tk * 4);
+    L.hscale = take(Tk * 4);
+  }
   if (fwd) L.y_partial = take(Tk * d.H * 2);
   L.total = off;
   return L;
@@ -194,15 +200,27 @@ moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const vo
                               const float *topk_w, void *y_partial, void *h16, uint32_t *status,
                               cudaStream_t stream);
 
-// NVFP4 or FP8 weights with bf16 x_perm and h [Tk, I]: weights dequantised
-// into tensor memory, token rows on the MMA's N side (experts_packed_wt.cu).
-// Used while the token tiles hold at most kPackedWtMaxRows rows.
+// NVFP4 or FP8 weights, small and mid-size batches: weights dequantised into
+// tensor memory, token rows on the MMA's N side, f16 operands with one
+// power-of-two scale per token row (experts_packed_wt.cu).  x_perm is bf16
+// [Tk, H]; x16 receives its scaled f16 copy (may equal x_perm: converted in
+// place); h [Tk, I] holds bf16 h, then its scaled f16 copy; xscale, hmax and
+// hscale are [Tk] scratch.  Used while the token tiles hold at most
+// kPackedWtMaxRows rows.
+struct PackedWtScratch {
+  void *x16;
+  void *h;
+  float *xscale;
+  uint32_t *hmax;
+  float *hscale;
+};
 constexpr int kPackedWtMaxRows = 64;
 bool packed_wt_applies(const moe_dims &d);
 moe_status launch_experts_packed_wt(const moe_dims &d, const moe_experts &ex, const void *x_perm,
                                     const int32_t *expert_offsets, const int32_t *row_src,
-                                    const float *topk_w, void *y_partial, __nv_bfloat16 *h,
-                                    uint32_t *status, cudaStream_t stream);
+                                    const float *topk_w, void *y_partial,
+                                    const PackedWtScratch &scr, uint32_t *status,
+                                    cudaStream_t stream);
 
 // bf16 [E, N, K] -> MMA-tiled layout (see moe_pack_bf16 in beam_moe.h).
 moe_status launch_pack_bf16(int E, int N, int K, const void *src, void *dst, cudaStream_t stream);

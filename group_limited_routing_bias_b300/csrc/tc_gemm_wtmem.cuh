@@ -3,20 +3,19 @@
 //
 // Each tile computes NA accumulators D_a[128 x BN] (fp32, tensor memory) =
 // W_a[128 x K] . X[BN x K]^T: 128 weight rows of one expert on the MMA's M
-// side (gate and up rows for NA = 2), the expert's token rows on N.  A
-// kind::f16 MMA with M = 128 costs the same ~45 clocks for any N up to 64
-// whether A sits in shared or in tensor memory, but with A in shared memory
-// the dequantised weights cross shared memory twice (the converters' store,
-// the MMA's read), ~4 bytes per weight, which caps the small-batch GEMMs
-// below HBM bandwidth.  Here the converters write the weights into tensor
-// memory with tcgen05.st; shared memory only carries the packed bytes and the
-// small activation tiles.
+// side (gate and up rows for NA = 2), the expert's token rows on N.  Issued
+// by an elected lane of a converged warp, a kind::f16 MMA with M = 128, N = 32
+// and A in tensor memory takes 16 clocks (N = 16: 9, N = 64: 32), the tensor
+// rate; with A in shared memory an N = 32 MMA takes 40 clocks, bound by
+// shared-memory reads of A, and the dequantised weights would cross shared
+// memory twice (the converters' store, the MMA's read).  Here the converters
+// write the weights into tensor memory with tcgen05.st; shared memory only
+// carries the packed bytes and the small activation tiles.
 //
 // The K loop runs in steps of KS 64-wide slices, KS * NA = 4 A tiles of 128
-// rows x 64 k per step.  The MMA thread's issue of a kind::f16 MMA blocks for
-// about as long as the tensor core takes to accept it (~45 clocks), and its
-// first barrier wait after a commit costs a few hundred clocks more, so each
-// step carries 16 MMAs per wait and commit.
+// rows x 64 k per step.  A barrier wait right after a commit costs a few
+// hundred clocks (it returns once the committed MMAs are done), so each step
+// carries 16 MMAs per wait and commit.
 //
 // One CTA per SM, persistent, 768 threads:
 //   warp 0 lane 0 : weight producer: each step's packed weights into a deep
@@ -25,7 +24,8 @@
 //                   token rows x 64 k, 128-byte swizzle, the MMA's B operand)
 //                   into a B ring of BS steps, freed by the MMA's commits, so
 //                   the activations are fetched well before the step is due
-//   warp 1 lane 0 : MMA issuer: tcgen05.mma kind::f16 with A from tensor
+//   warp 1        : MMA issuer, converged, one elected lane issuing:
+//                   tcgen05.mma kind::f16 (f16 operands) with A from tensor
 //                   memory; one wait and one commit per step
 //   warp 2        : tensor-memory allocation / release (all 512 columns)
 //   warps 4..7    : epilogue; warp 4+q reads accumulator rows 32q..32q+31
@@ -35,14 +35,14 @@
 //                   quarter q) into 32 columns of the stage.  After the B tiles
 //                   have landed too, the group signals the stage full.
 // Tensor memory: accumulators [0, NBUF * NA * BN); then AST stages of
-// 4 * 32 columns (four A tiles of 128 rows x 64 k in bf16 pairs).
+// 4 * 32 columns (four A tiles of 128 rows x 64 k in f16 pairs).
 //
 // Every wait is bounded (ptx.cuh); on expiry the CTA records MOE_DEV_TIMEOUT,
 // lets its copies and MMAs drain, frees tensor memory and returns.
 //
 // A problem class P supplies:
 //   static constexpr int BN, NA, KS, NBUF, AST, RS, BS, RAW_BYTES;   (RAW_BYTES: one step)
-//   static constexpr bool DYNAMIC, PDL_PRIMARY, PDL_SECONDARY;
+//   static constexpr bool DYNAMIC, PDL_PRIMARY, PDL_SECONDARY, PDL_WAIT_B;
 //   struct Params { ...; uint32_t *status; uint32_t *sched_counters; };
 //   struct Sched; struct Tile;
 //   static void prologue(const Params&, Sched&)
@@ -55,7 +55,7 @@
 //   static void load_raw(const Params&, const Tile&, int s, uint8_t *raw, uint64_t *bar)
 //   static void convert_row(const Params&, const Tile&, int s, const uint8_t *raw, int j,
 //                           int a, int row, uint32_t (&out)[32])
-//                                       (slice j of the step, matrix a: bf16 pairs of 64 k)
+//                                       (slice j of the step, matrix a: f16 pairs of 64 k)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
 //   optional tile_ready / tile_done / last_cta hooks as in tc_gemm.cuh.
 #pragma once
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
   constexpr uint32_t kACol0 = P::NBUF * kAccCols;
   constexpr uint32_t kStageCols = kWtTilesPerStep * 32;
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, BN);
+  constexpr uint32_t kIdesc = umma_idesc_f16(kTileM, BN);
   constexpr bool DYN = P::DYNAMIC;
   static_assert(KS * NA == kWtTilesPerStep, "a step holds four A tiles");
   static_assert(kACol0 + AST * kStageCols <= kTmemCols, "tensor memory overflow");
@@ -247,7 +247,10 @@ __global__ void __launch_bounds__(kWtThreads, 1)
   } else if (warp == 3) {
     if (lane == 0) {
       // ---------------- activation producer (a down tile's h rows are read only
-      // once tile_ready says its expert's gate/up tiles have published them)
+      // once tile_ready says they have been published; with PDL_WAIT_B the
+      // activations are the previous launch's output: this thread alone waits
+      // for it to complete, while the weights already stream and convert)
+      if constexpr (P::PDL_WAIT_B) asm volatile("griddepcontrol.wait;" ::: "memory");
       int bs = 0, cur = blockIdx.x, tslot = 0;
       uint32_t ph = 0, issued = 0, par = 0, tph = 0;
       bool ok = true;
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
               for (int kk = 0; kk < kTileK / 16; ++kk) {
 #pragma unroll
                 for (int a = 0; a < NA; ++a)
-                  umma_bf16_tmem_a(d0 + a * BN, acol + (j * NA + a) * 32 + 8 * kk, bdesc + 2 * kk,
+                  umma_f16_tmem_a(d0 + a * BN, acol + (j * NA + a) * 32 + 8 * kk, bdesc + 2 * kk,
                                    kIdesc, (s | j | kk) != 0 ? 1u : 0u);
               }
             }
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       __syncwarp();
     }
   } else if (warp >= 8) {
-    // ---------------- converters: packed weights -> bf16 A stages in tensor memory
+    // ---------------- converters: packed weights -> f16 A stages in tensor memory
     const int g = (warp - 8) >> 2;  // warpgroup = A tile of the step
     const int q = warp & 3;         // tensor-memory lane quarter
     const int row = q * 32 + lane;
