@@ -40,19 +40,20 @@ namespace beam {
 
 namespace {
 
-// One NVFP4 weight row of a 64-wide K slice: 32 code bytes (even k in the low
-// nibble) and the four e4m3 scales of its 16-k blocks -> 32 f16 pairs.
-__device__ __forceinline__ void nvfp4_row_f16(uint4 c0, uint4 c1, uint32_t scales,
-                                              uint32_t (&out)[32]) {
-  uint32_t s16[4];
+// Half h of one NVFP4 weight row of a 64-wide K slice: 16 code bytes (k 32h ..
+// 32h + 31, even k in the low nibble) and the e4m3 scales of its two 16-k
+// blocks (bytes 2h, 2h + 1 of `scales`) -> 16 f16 pairs.
+__device__ __forceinline__ void nvfp4_half_f16(uint4 c, uint32_t scales, int h,
+                                               uint32_t (&out)[16]) {
+  uint32_t s16[2];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint32_t byte = (scales >> (8 * b)) & 0xFFu;
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t byte = (scales >> (8 * (2 * h + b))) & 0xFFu;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16[b]) : "h"((uint16_t)(byte | (byte << 8))));
   }
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {  // word i: k 8i .. 8i + 7, block i / 2
+  for (int i = 0; i < 4; ++i) {  // word i: k 32h + 8i .. + 7, block i / 2 of the half
     uint32_t h0, h1, h2, h3;
     asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
         "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
@@ -62,19 +63,19 @@ __device__ __forceinline__ void nvfp4_row_f16(uint4 c0, uint4 c1, uint32_t scale
         "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
         : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
         : "r"(w[i]));
-    const uint32_t s = s16[i >> 1];
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 0]) : "r"(h0), "r"(s));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 1]) : "r"(h1), "r"(s));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 2]) : "r"(h2), "r"(s));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 3]) : "r"(h3), "r"(s));
+    const uint32_t sc = s16[i >> 1];
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 0]) : "r"(h0), "r"(sc));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 1]) : "r"(h1), "r"(sc));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 2]) : "r"(h2), "r"(sc));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(out[4 * i + 3]) : "r"(h3), "r"(sc));
   }
 }
 
-// One FP8 weight row of a 64-wide K slice: 64 e4m3 codes -> 32 f16 pairs.
-__device__ __forceinline__ void fp8_row_f16(const uint8_t *codes, uint32_t (&out)[32]) {
+// Half h of one FP8 weight row of a 64-wide K slice: 32 e4m3 codes -> 16 f16 pairs.
+__device__ __forceinline__ void fp8_half_f16(const uint8_t *codes, int h, uint32_t (&out)[16]) {
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 q = *reinterpret_cast<const uint4 *>(codes + 16 * v);
+  for (int v = 0; v < 2; ++v) {
+    const uint4 q = *reinterpret_cast<const uint4 *>(codes + 32 * h + 16 * v);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -213,28 +214,28 @@ __global__ void __launch_bounds__(128) h_rows_f16_scaled_kernel(
 struct WtNvfp4 {
   static constexpr bool kTiled = false, kPerRowScale = false;
   static constexpr int kTileBytes = 128 * 48;
-  __device__ static void convert(const uint8_t *t, int k, int r, uint32_t (&out)[32]) {
-    const uint4 *c = reinterpret_cast<const uint4 *>(t + r * 32);
+  __device__ static void convert(const uint8_t *t, int k, int r, int h, uint32_t (&out)[16]) {
+    const uint4 c = reinterpret_cast<const uint4 *>(t + r * 32)[h];
     const uint32_t sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 16 + (k & 3) * 4);
-    nvfp4_row_f16(c[0], c[1], sc, out);
+    nvfp4_half_f16(c, sc, h, out);
   }
 };
 // Tiled NVFP4 (moe_pack_nvfp4): codes [128][32 B], then scales [128][4 B].
 struct WtNvfp4Tiled {
   static constexpr bool kTiled = true, kPerRowScale = false;
   static constexpr int kTileBytes = 4608;
-  __device__ static void convert(const uint8_t *t, int, int r, uint32_t (&out)[32]) {
-    const uint4 *c = reinterpret_cast<const uint4 *>(t + r * 32);
+  __device__ static void convert(const uint8_t *t, int, int r, int h, uint32_t (&out)[16]) {
+    const uint4 c = reinterpret_cast<const uint4 *>(t + r * 32)[h];
     const uint32_t sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 4);
-    nvfp4_row_f16(c[0], c[1], sc, out);
+    nvfp4_half_f16(c, sc, h, out);
   }
 };
 // FP8, row-major (TMA box) or tiled (moe_pack_fp8): codes [128][64 B].
 struct WtFp8 {
   static constexpr bool kTiled = false, kPerRowScale = true;
   static constexpr int kTileBytes = 8192;
-  __device__ static void convert(const uint8_t *t, int, int r, uint32_t (&out)[32]) {
-    fp8_row_f16(t + r * 64, out);
+  __device__ static void convert(const uint8_t *t, int, int r, int h, uint32_t (&out)[16]) {
+    fp8_half_f16(t + r * 64, h, out);
   }
 };
 struct WtFp8Tiled : WtFp8 {
@@ -351,8 +352,8 @@ struct ExpertGemmWT {
     }
   }
   __device__ static void convert_row(const Params &, const Tile &, int s, const uint8_t *raw,
-                                     int j, int a, int row, uint32_t (&out)[32]) {
-    Fmt::convert(raw + (j * NA + a) * Fmt::kTileBytes, s * KS + j, row, out);
+                                     int j, int a, int row, int h, uint32_t (&out)[16]) {
+    Fmt::convert(raw + (j * NA + a) * Fmt::kTileBytes, s * KS + j, row, h, out);
   }
   // gate/up: each epilogue warp counts its 32 features of h for the tile (its
   // stores and row maxima before the count); the h rescaling kernel waits for

@@ -54,8 +54,9 @@
 //                                       (KS tiles of BN rows x 128 bytes)
 //   static void load_raw(const Params&, const Tile&, int s, uint8_t *raw, uint64_t *bar)
 //   static void convert_row(const Params&, const Tile&, int s, const uint8_t *raw, int j,
-//                           int a, int row, uint32_t (&out)[32])
-//                                       (slice j of the step, matrix a: f16 pairs of 64 k)
+//                           int a, int row, int h, uint32_t (&out)[16])
+//                                       (slice j of the step, matrix a, half h: f16
+//                                        pairs of k 32h .. 32h + 31)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
 //   optional tile_ready / tile_done / last_cta hooks as in tc_gemm.cuh.
 #pragma once
@@ -383,11 +384,15 @@ __global__ void __launch_bounds__(kWtThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t v[32];
-        P::convert_row(p, tile, s, raws + rs * P::RAW_BYTES, j, a, row, v);
+        // two halves of 32 k: the first half's store runs while the second
+        // half converts
+        uint32_t v[16];
+        P::convert_row(p, tile, s, raws + rs * P::RAW_BYTES, j, a, row, 0, v);
+        tmem_st16(tq + as * kStageCols, v);
+        P::convert_row(p, tile, s, raws + rs * P::RAW_BYTES, j, a, row, 1, v);
+        tmem_st16(tq + as * kStageCols + 16, v);
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rs]);  // the packed bytes are in registers
-        tmem_st32(tq + as * kStageCols, v);
         tmem_wait_st();
         // the stage is complete for the MMA once its B tiles have landed too:
         // one warp checks (the stage completes only with every warp's arrival,
