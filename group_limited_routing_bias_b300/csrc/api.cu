@@ -270,18 +270,17 @@ moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts, 
     return launch_experts_w4a4(*dims, *experts, xq, xs, expert_offsets, row_src, topk_w, y_partial,
                                at<uint8_t>(ws, L.hq), at<uint8_t>(ws, L.hs), status_word(ws), s);
   }
-  if (experts->dtype != MOE_W_BF16 && packed_wt_applies(*dims)) {
+  if (experts->dtype != MOE_W_BF16) {
     const PackedWtScratch scr{at<void>(ws, L.x16), at<void>(ws, L.h), at<float>(ws, L.xscale),
                               at<uint32_t>(ws, L.hmax), at<float>(ws, L.hscale)};
-    return launch_experts_packed_wt(*dims, *experts, x_perm, expert_offsets, row_src, topk_w,
-                                    y_partial, scr, status_word(ws), s);
-  }
-  if (experts->dtype != MOE_W_BF16) {
-    void *x16 = at<void>(ws, L.x16);
-    const size_t n = (size_t)dims->T * dims->top_k * dims->H;
-    if ((st = launch_bf16_to_f16(x_perm, x16, n, s)) != MOE_OK) return st;
-    return launch_experts_fp4(*dims, *experts, x16, expert_offsets, row_src, topk_w, y_partial,
-                              at<void>(ws, L.h), status_word(ws), s);
+    if (packed_wt_applies(*dims))
+      return launch_experts_packed_wt(*dims, *experts, x_perm, expert_offsets, row_src, topk_w,
+                                      y_partial, scr, status_word(ws), s);
+    if ((st = launch_rows_f16_scaled(x_perm, scr.x16, (long)dims->T * dims->top_k, dims->H,
+                                     scr.xscale, scr.hmax, s)) != MOE_OK)
+      return st;
+    return launch_experts_fp4(*dims, *experts, expert_offsets, row_src, topk_w, y_partial, scr,
+                              status_word(ws), s);
   }
   return launch_experts(*dims, *experts, x_perm, expert_offsets, row_src, topk_w, y_partial,
                         at<__nv_bfloat16>(ws, L.h), status_word(ws), s);
@@ -311,9 +310,9 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   const WsLayout L = ws_layout(d, MOE_OP_FORWARD, experts->dtype);
   const bool a4 = experts->dtype == MOE_W_NVFP4_A4;
   const bool packed = experts->dtype != MOE_W_BF16 && !a4;
-  // packed weights: small and mid-size batches dequantise into tensor memory
-  // (activations as f16 with a power-of-two scale per row); large ones run the
-  // token-major GEMMs on plain f16 activations
+  // packed weights: small and mid-size batches dequantise into tensor memory,
+  // large ones run the token-major GEMMs; both on f16 activations with a
+  // power-of-two scale per row
   const bool packed_wt = packed && packed_wt_applies(d);
   const bool fp4 = packed && !packed_wt;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -327,12 +326,13 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
   int32_t *offsets = at<int32_t>(ws, L.offsets);
   int32_t *slot_of = at<int32_t>(ws, L.slot_of);
   int32_t *row_src = at<int32_t>(ws, L.row_src);
-  // the gather writes x_perm in the GEMMs' operand type: bf16, or f16 for the
+  // the gather writes x_perm in bf16, or as f16 scaled per token for the
   // token-major packed-weight GEMMs; W4A4 quantises each token once and
   // writes it to its slots
-  const GatherMode gm = a4 ? kGatherNone : fp4 ? kGatherF16 : kGatherBf16;
+  const GatherMode gm = a4 ? kGatherNone : fp4 ? kGatherF16Scaled : kGatherBf16;
   if ((st = launch_permute(d, idx, x, x_perm, offsets, slot_of, row_src, at<int32_t>(ws, L.counts),
-                           at<int32_t>(ws, L.bases), status, s, gm)) != MOE_OK)
+                           at<int32_t>(ws, L.bases), status, s, gm, at<float>(ws, L.xscale),
+                           at<uint32_t>(ws, L.hmax))) != MOE_OK)
     return st;
   void *y_partial = at<void>(ws, L.y_partial);
   if (a4) {
@@ -349,9 +349,11 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
     st = launch_experts_packed_wt(d, *experts, x_perm, offsets, row_src, w, y_partial, scr, status,
                                   s);
   }
-  else if (fp4)
-    st = launch_experts_fp4(d, *experts, x_perm, offsets, row_src, w, y_partial, at<void>(ws, L.h),
-                            status, s);
+  else if (fp4) {
+    const PackedWtScratch scr{x_perm, at<void>(ws, L.h), at<float>(ws, L.xscale),
+                              at<uint32_t>(ws, L.hmax), at<float>(ws, L.hscale)};
+    st = launch_experts_fp4(d, *experts, offsets, row_src, w, y_partial, scr, status, s);
+  }
   else
     st = launch_experts(d, *experts, x_perm, offsets, row_src, w, y_partial,
                         at<__nv_bfloat16>(ws, L.h), status, s);

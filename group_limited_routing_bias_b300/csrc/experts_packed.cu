@@ -18,16 +18,21 @@
 // eight converter warps turn each 64-wide K slice into an f16 operand tile
 // with the 128-byte swizzle (hardware e2m1x2 and e4m3x2 conversions, one
 // f16x2 multiply per code pair) and free the raw slot at once, and the
-// activations (exact bf16 -> f16 copies, made in the dispatch gather) arrive
-// by TMA.  h is kept in f16.
+// activations arrive by TMA as f16 rows scaled by a power of two each
+// (rowscale.cuh): x_perm scaled in the dispatch gather, h written in bf16
+// with its row maxima by the gate/up epilogue, then rescaled in place by a
+// small kernel between the two GEMMs.  The epilogues multiply each row's
+// inverse factor back into the accumulator.
 //
 // Two tile shapes: token rows on M with 256 weight rows on N (from 64 token
-// rows per call up, decode included), and weights on M with the tokens on N
-// for the smallest batches.  Both stream each touched expert's packed weights
-// once per token tile.
+// rows per call up), and weights on M with the tokens on N for the smallest
+// batches.  Both stream each touched expert's packed weights once per token
+// tile.  (Batches whose expert tiles hold at most 64 rows run the
+// tensor-memory GEMMs of experts_packed_wt.cu instead.)
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
+#include "rowscale.cuh"
 #include "sched.cuh"
 #include "tc_gemm.cuh"
 
@@ -182,11 +187,6 @@ __device__ __forceinline__ void load_tile(uint8_t *raw, const uint8_t *w, int rb
   bulk_load(raw, w + ((size_t)rblk * ktiles + k) * Fmt::kTileBytes, Fmt::kTileBytes, bar);
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&v);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2_(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&v);
@@ -219,7 +219,9 @@ struct Fp4Params {
   const int32_t *offsets;
   const int32_t *row_src;
   const float *topk_w;
-  void *out;  // h f16 [Tk, I] or y_partial bf16 [Tk, H]
+  void *out;  // h bf16 [Tk, I] or y_partial bf16 [Tk, H]
+  const float *bscale;  // [Tk] inverse row factor of the activations (x16 or h, rowscale.cuh)
+  uint32_t *hmax;       // [Tk] gate/up: largest |h| of each row (fp32 bits)
   int E, out_cols, w_rows, ksteps, mt;
   uint32_t *status;
 };
@@ -295,14 +297,22 @@ struct ExpertGemmFP4 {
         uint32_t u[CH];
         tmem_ld_n<CH>(taddr + BN + c, u);
         tmem_wait_ld();
-        __half *out = static_cast<__half *>(p.out);
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
+          uint32_t mag = 0;
           if (c + j < t.nrows) {
-            const float gv = __uint_as_float(a[j]) * ga;
-            const float hv = gv / (1.0f + __expf(-gv)) * (__uint_as_float(u[j]) * gb);
-            out[(size_t)(t.row0 + c + j) * p.out_cols + f] = __float2half_rn(hv);
+            const int r = t.row0 + c + j;
+            const float bs = __ldg(p.bscale + r);
+            const float gv = __uint_as_float(a[j]) * bs * ga;
+            const float hv = gv / (1.0f + __expf(-gv)) * (__uint_as_float(u[j]) * bs * gb);
+            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+            out[(size_t)r * p.out_cols + f] = hb;
+            mag = __float_as_uint(fabsf(__bfloat162float(hb)));
           }
+          // the row's largest |h| over this warp's 32 features, one atomic per row
+          mag = __reduce_max_sync(0xffffffffu, mag);
+          if ((row & 31) == j && c + j < t.nrows) atomicMax(p.hmax + t.row0 + c + j, mag);
         }
       } else {
         tmem_wait_ld();
@@ -312,7 +322,8 @@ struct ExpertGemmFP4 {
           if (c + j < t.nrows) {
             const int r = t.row0 + c + j;
             const float w = __ldg(p.topk_w + __ldg(p.row_src + r)) * ga;
-            out[(size_t)r * p.out_cols + f] = __float2bfloat16_rn(__uint_as_float(a[j]) * w);
+            out[(size_t)r * p.out_cols + f] =
+                __float2bfloat16_rn(__uint_as_float(a[j]) * __ldg(p.bscale + r) * w);
           }
         }
       }
@@ -338,6 +349,12 @@ struct ExpertGemmTMFP4 {
   static constexpr int RSTAGES = (RSTAGES_FIT > 16 ? 16 : RSTAGES_FIT) / CGROUPS * CGROUPS;
   static_assert(RSTAGES >= 2, "raw ring needs two slots");
   static constexpr int FW = GATEUP ? 128 : 256;
+  // gate/up -> h rescaling -> down, each a programmatic dependent of the one
+  // before: down streams and converts weights at once, its activation
+  // producer waits for the rescaled h
+  static constexpr bool PDL_PRIMARY = GATEUP;
+  static constexpr bool PDL_SECONDARY = !GATEUP;
+  static constexpr bool PDL_WAIT_B = !GATEUP;
 
   using Params = Fp4Params;
   using Sched = TileSched;
@@ -389,8 +406,12 @@ struct ExpertGemmTMFP4 {
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     const bool valid = row < t.nrows;
     const int n0 = t.f * FW;  // first output feature of the tile
+    // this thread's token row: its inverse activation factor (rowscale.cuh)
+    const float bs = valid ? __ldg(p.bscale + t.row0 + row) : 0.f;
     if (GATEUP) {
-      __half *dst = static_cast<__half *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + n0;
+      __nv_bfloat16 *dst =
+          static_cast<__nv_bfloat16 *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + n0;
+      float hmax = 0.f;
 #pragma unroll 1
       for (int c = 0; c < FW; c += 32) {
         uint32_t g[32], u[32];
@@ -402,19 +423,24 @@ struct ExpertGemmTMFP4 {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int n = n0 + c + 2 * j;
-            const float g0 = __uint_as_float(g[2 * j]) * weight_scale(p.g0, p.scale_rows, t.e, n);
-            const float g1 = __uint_as_float(g[2 * j + 1]) * weight_scale(p.g0, p.scale_rows, t.e, n + 1);
+            const float g0 = __uint_as_float(g[2 * j]) * bs * weight_scale(p.g0, p.scale_rows, t.e, n);
+            const float g1 =
+                __uint_as_float(g[2 * j + 1]) * bs * weight_scale(p.g0, p.scale_rows, t.e, n + 1);
             const float h0 = g0 / (1.0f + __expf(-g0)) *
-                             (__uint_as_float(u[2 * j]) * weight_scale(p.g1, p.scale_rows, t.e, n));
+                             (__uint_as_float(u[2 * j]) * bs * weight_scale(p.g1, p.scale_rows, t.e, n));
             const float h1 = g1 / (1.0f + __expf(-g1)) *
-                             (__uint_as_float(u[2 * j + 1]) * weight_scale(p.g1, p.scale_rows, t.e, n + 1));
-            pk[j] = pack_f16x2(h0, h1);
+                             (__uint_as_float(u[2 * j + 1]) * bs *
+                              weight_scale(p.g1, p.scale_rows, t.e, n + 1));
+            pk[j] = pack_bf16x2_(h0, h1);
+            const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162 *>(&pk[j]);
+            hmax = fmaxf(hmax, fmaxf(fabsf(__low2float(hb)), fabsf(__high2float(hb))));
           }
           uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
           for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
+      if (valid) atomicMax(p.hmax + t.row0 + row, __float_as_uint(hmax));
     } else {
       const float w = valid ? __ldg(p.topk_w + __ldg(p.row_src + t.row0 + row)) : 0.f;
       __nv_bfloat16 *dst =
@@ -429,9 +455,9 @@ struct ExpertGemmTMFP4 {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int n = n0 + c + 2 * j;
-            pk[j] = pack_bf16x2_(__uint_as_float(a[2 * j]) * w * weight_scale(p.g0, p.scale_rows, t.e, n),
-                                 __uint_as_float(a[2 * j + 1]) * w *
-                                     weight_scale(p.g0, p.scale_rows, t.e, n + 1));
+            pk[j] = pack_bf16x2_(
+                __uint_as_float(a[2 * j]) * bs * w * weight_scale(p.g0, p.scale_rows, t.e, n),
+                __uint_as_float(a[2 * j + 1]) * bs * w * weight_scale(p.g0, p.scale_rows, t.e, n + 1));
           }
           uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
@@ -449,7 +475,51 @@ moe_status launch_fp4(const Fp4Params &prm, int grid, cudaStream_t stream) {
   constexpr int smem = smem_bytes_for<P>();
   static_assert(smem <= kSmemLimit, "shared memory budget");
   if (ensure_smem_limit((const void *)tc_gemm_kernel<P>, smem) != MOE_OK) return MOE_ERR_CUDA;
-  tc_gemm_kernel<P><<<grid, threads_for<P>(), smem, stream>>>(prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads_for<P>());
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PdlSecondaryOf<P>::value ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel<P>, prm) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Rows of h (bf16 [rows, K], in place) -> f16 scaled per row by the factor
+// the gate/up epilogues' maxima ask for (rowscale.cuh); hscale[r] receives
+// the inverse factor.  A programmatic dependent of gate/up: it lets the down
+// GEMM's launch begin, then waits for gate/up to complete.  One warp per row.
+__global__ void __launch_bounds__(256) h_rows_rescale_kernel(__nv_bfloat16 *h, long rows, int K,
+                                                             const uint32_t *hmax, float *hscale) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  for (long r = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const float inv = rescale_row_inplace(h + r * K, K, __ldcg(hmax + r), lane);
+    if (lane == 0) hscale[r] = inv;
+  }
+}
+
+moe_status launch_h_rescale(const moe_dims &d, const PackedWtScratch &scr, cudaStream_t stream) {
+  const long Tk = (long)d.T * d.top_k;
+  const int grid = (int)std::max<long>(1, std::min<long>((Tk + 7) / 8, (long)device_sm_count() * 8));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, h_rows_rescale_kernel, static_cast<__nv_bfloat16 *>(scr.h), Tk, d.I,
+                         (const uint32_t *)scr.hmax, scr.hscale) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -510,22 +580,24 @@ Fp4Params base_params(const moe_dims &d, const int32_t *offsets, const int32_t *
 }
 
 template <class Fmt, int BN>
-moe_status launch_packed_small(const moe_dims &d, const moe_experts &ex, const void *x16,
-                               const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                               void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+moe_status launch_packed_small(const moe_dims &d, const moe_experts &ex, const int32_t *offsets,
+                               const int32_t *row_src, const float *topk_w, void *y_partial,
+                               const PackedWtScratch &scr, uint32_t *status, cudaStream_t stream) {
   const long Tk = (long)d.T * d.top_k;
   const long max_tt = Tk / BN + std::min<long>(d.E, Tk);
   const int sms = device_sm_count();
   {
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.I;
-    if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, BN) ||
+    if (!make_act_map(&prm.tmap_act, scr.x16, d.H, Tk, BN) ||
         !set_weights<Fmt>(prm, ex.w_gate, ex.s_gate, ex.w_up, ex.s_up, d.H, rows, kTileM))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_gate;
     prm.g1 = ex.g_up;
     prm.scale_rows = Fmt::kPerRowScale ? d.I : 0;
-    prm.out = h16;
+    prm.out = scr.h;
+    prm.bscale = scr.xscale;
+    prm.hmax = scr.hmax;
     prm.out_cols = d.I;
     prm.w_rows = d.I;
     prm.ksteps = d.H / kTileK;
@@ -534,16 +606,18 @@ moe_status launch_packed_small(const moe_dims &d, const moe_experts &ex, const v
     const moe_status st = launch_fp4<ExpertGemmFP4<Fmt, BN, true>>(prm, grid, stream);
     if (st != MOE_OK) return st;
   }
+  if (launch_h_rescale(d, scr, stream) != MOE_OK) return MOE_ERR_CUDA;
   {
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.H;
-    if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, BN) ||
+    if (!make_act_map(&prm.tmap_act, scr.h, d.I, Tk, BN) ||
         !set_weights<Fmt>(prm, ex.w_down, ex.s_down, ex.w_down, ex.s_down, d.I, rows, kTileM))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_down;
     prm.g1 = ex.g_down;
     prm.scale_rows = Fmt::kPerRowScale ? d.H : 0;
     prm.out = y_partial;
+    prm.bscale = scr.hscale;
     prm.out_cols = d.H;
     prm.w_rows = d.H;
     prm.ksteps = d.I / kTileK;
@@ -554,9 +628,9 @@ moe_status launch_packed_small(const moe_dims &d, const moe_experts &ex, const v
 }
 
 template <class Fmt>
-moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const void *x16,
-                               const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                               void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const int32_t *offsets,
+                               const int32_t *row_src, const float *topk_w, void *y_partial,
+                               const PackedWtScratch &scr, uint32_t *status, cudaStream_t stream) {
   const long Tk = (long)d.T * d.top_k;
   const long max_tt = Tk / kTileM + std::min<long>(d.E, Tk);
   const int sms = device_sm_count();
@@ -564,15 +638,17 @@ moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const v
     using P = ExpertGemmTMFP4<Fmt, true>;
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.I;
-    if (!make_act_map(&prm.tmap_act, x16, d.H, Tk, kTileM) ||
-        !make_act_map(&prm.tmap_act32, x16, d.H, Tk, 32) ||
-        !make_act_map(&prm.tmap_act64, x16, d.H, Tk, 64) ||
+    if (!make_act_map(&prm.tmap_act, scr.x16, d.H, Tk, kTileM) ||
+        !make_act_map(&prm.tmap_act32, scr.x16, d.H, Tk, 32) ||
+        !make_act_map(&prm.tmap_act64, scr.x16, d.H, Tk, 64) ||
         !set_weights<Fmt>(prm, ex.w_gate, ex.s_gate, ex.w_up, ex.s_up, d.H, rows, 128))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_gate;
     prm.g1 = ex.g_up;
     prm.scale_rows = Fmt::kPerRowScale ? d.I : 0;
-    prm.out = h16;
+    prm.out = scr.h;
+    prm.bscale = scr.xscale;
+    prm.hmax = scr.hmax;
     prm.out_cols = d.I;
     prm.w_rows = d.I;
     prm.ksteps = d.H / kTileK;
@@ -581,19 +657,21 @@ moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const v
     const moe_status st = launch_fp4<P>(prm, grid, stream);
     if (st != MOE_OK) return st;
   }
+  if (launch_h_rescale(d, scr, stream) != MOE_OK) return MOE_ERR_CUDA;
   {
     using P = ExpertGemmTMFP4<Fmt, false>;
     Fp4Params prm = base_params(d, offsets, row_src, topk_w, status);
     const long rows = (long)d.E * d.H;
-    if (!make_act_map(&prm.tmap_act, h16, d.I, Tk, kTileM) ||
-        !make_act_map(&prm.tmap_act32, h16, d.I, Tk, 32) ||
-        !make_act_map(&prm.tmap_act64, h16, d.I, Tk, 64) ||
+    if (!make_act_map(&prm.tmap_act, scr.h, d.I, Tk, kTileM) ||
+        !make_act_map(&prm.tmap_act32, scr.h, d.I, Tk, 32) ||
+        !make_act_map(&prm.tmap_act64, scr.h, d.I, Tk, 64) ||
         !set_weights<Fmt>(prm, ex.w_down, ex.s_down, ex.w_down, ex.s_down, d.I, rows, 256))
       return MOE_ERR_CUDA;
     prm.g0 = ex.g_down;
     prm.g1 = ex.g_down;
     prm.scale_rows = Fmt::kPerRowScale ? d.H : 0;
     prm.out = y_partial;
+    prm.bscale = scr.hscale;
     prm.out_cols = d.H;
     prm.w_rows = d.H;
     prm.ksteps = d.I / kTileK;
@@ -604,58 +682,41 @@ moe_status launch_packed_large(const moe_dims &d, const moe_experts &ex, const v
 }
 
 template <class Fmt>
-moe_status launch_packed(const moe_dims &d, const moe_experts &ex, const void *x16,
-                         const int32_t *offsets, const int32_t *row_src, const float *topk_w,
-                         void *y_partial, void *h16, uint32_t *status, cudaStream_t stream) {
+moe_status launch_packed(const moe_dims &d, const moe_experts &ex, const int32_t *offsets,
+                         const int32_t *row_src, const float *topk_w, void *y_partial,
+                         const PackedWtScratch &scr, uint32_t *status, cudaStream_t stream) {
   // Token-major tiles from 64 (token, expert) rows up: with the weights on N
   // one MMA covers 256 weight rows, and the converter groups keep two K slices
   // in flight.  Measured on B300 (expert stage, tiled NVFP4): 0.94 vs 1.07 ms
   // at T=64 (top-8), 1.35 vs 2.11 ms at T=256, 1.88 vs 3.61 ms at T=1024; the
   // weights-on-M tiles stay for the smallest batches (T=1: 0.14 vs 0.17 ms).
   if ((long)d.T * d.top_k >= 64 && d.H % 256 == 0)
-    return launch_packed_large<Fmt>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status,
-                                    stream);
+    return launch_packed_large<Fmt>(d, ex, offsets, row_src, topk_w, y_partial, scr, status, stream);
   switch (expert_bn(d)) {
-    case 16: return launch_packed_small<Fmt, 16>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
-    case 32: return launch_packed_small<Fmt, 32>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
-    case 64: return launch_packed_small<Fmt, 64>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
-    case 128: return launch_packed_small<Fmt, 128>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
-    default: return launch_packed_small<Fmt, 256>(d, ex, x16, offsets, row_src, topk_w, y_partial, h16, status, stream);
+    case 16: return launch_packed_small<Fmt, 16>(d, ex, offsets, row_src, topk_w, y_partial, scr, status, stream);
+    case 32: return launch_packed_small<Fmt, 32>(d, ex, offsets, row_src, topk_w, y_partial, scr, status, stream);
+    case 64: return launch_packed_small<Fmt, 64>(d, ex, offsets, row_src, topk_w, y_partial, scr, status, stream);
+    case 128: return launch_packed_small<Fmt, 128>(d, ex, offsets, row_src, topk_w, y_partial, scr, status, stream);
+    default: return launch_packed_small<Fmt, 256>(d, ex, offsets, row_src, topk_w, y_partial, scr, status, stream);
   }
-}
-
-__global__ void bf16_to_f16_kernel(const __nv_bfloat162 *__restrict__ in, __half2 *__restrict__ out,
-                                   size_t n2) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n2;
-       i += (size_t)gridDim.x * blockDim.x)
-    out[i] = __float22half2_rn(__bfloat1622float2(in[i]));
 }
 
 }  // namespace
 
-moe_status launch_bf16_to_f16(const void *in, void *out, size_t n, cudaStream_t stream) {
-  const size_t n2 = n / 2;
-  if (n2 == 0) return MOE_OK;
-  const int blocks = (int)std::min<size_t>((n2 + 255) / 256, (size_t)device_sm_count() * 16);
-  bf16_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat162 *>(in),
-                                                 static_cast<__half2 *>(out), n2);
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const void *x16,
+moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex,
                               const int32_t *expert_offsets, const int32_t *row_src,
-                              const float *topk_w, void *y_partial, void *h16, uint32_t *status,
-                              cudaStream_t stream) {
+                              const float *topk_w, void *y_partial, const PackedWtScratch &scr,
+                              uint32_t *status, cudaStream_t stream) {
   const bool tiled = ex.layout == MOE_LAYOUT_TILED;
   if (ex.dtype == MOE_W_FP8)
-    return tiled ? launch_packed<Fp8TiledFormat>(d, ex, x16, expert_offsets, row_src, topk_w,
-                                                 y_partial, h16, status, stream)
-                 : launch_packed<Fp8Format>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial,
-                                            h16, status, stream);
-  return tiled ? launch_packed<Nvfp4TiledFormat>(d, ex, x16, expert_offsets, row_src, topk_w,
-                                                 y_partial, h16, status, stream)
-               : launch_packed<Nvfp4Format>(d, ex, x16, expert_offsets, row_src, topk_w, y_partial,
-                                            h16, status, stream);
+    return tiled ? launch_packed<Fp8TiledFormat>(d, ex, expert_offsets, row_src, topk_w, y_partial,
+                                                 scr, status, stream)
+                 : launch_packed<Fp8Format>(d, ex, expert_offsets, row_src, topk_w, y_partial, scr,
+                                            status, stream);
+  return tiled ? launch_packed<Nvfp4TiledFormat>(d, ex, expert_offsets, row_src, topk_w, y_partial,
+                                                 scr, status, stream)
+               : launch_packed<Nvfp4Format>(d, ex, expert_offsets, row_src, topk_w, y_partial, scr,
+                                            status, stream);
 }
 
 }  // namespace beam

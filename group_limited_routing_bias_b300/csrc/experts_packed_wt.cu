@@ -12,16 +12,9 @@
 // converter thread dequantises one weight row of a 64-wide K slice, e2m1 (or
 // e4m3) pairs to f16 pairs by the hardware conversion, times the f16 block
 // scale (exact).  The activations keep bf16's range through one power-of-two
-// scale per token row: each row of x_perm, and each row of h once its expert's
-// gate/up tiles are all done, is multiplied by the power of two that puts its
-// largest magnitude in [2^14, 2^15) and stored as f16.  Every bf16 value of
-// the row is then exact in f16, except values below 2^-28 of the row's
-// largest, which become f16 subnormals (absolute error at most 2^-39 of it).
-// The MMAs see the scaled rows, so each accumulator column carries its row's
-// factor; the epilogue multiplies it back out (exactly, a power of two)
-// together with the NVFP4 global or the FP8 row scale.  The products are
-// exact and the tensor cores' accumulation is invariant under such a scaling,
-// so the results are those of bf16 operands.
+// scale per token row (rowscale.cuh): the epilogue multiplies each
+// accumulator column by its row's inverse factor, together with the NVFP4
+// global or the FP8 row scale.
 //
 // Tiles are taken from a global counter as in the bf16 weights-on-M GEMMs of
 // experts.cu.  The gate/up epilogue writes bf16 h and gathers each row's
@@ -33,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
+#include "rowscale.cuh"
 #include "sched.cuh"
 #include "tc_gemm_wtmem.cuh"
 
@@ -85,26 +79,6 @@ __device__ __forceinline__ void fp8_half_f16(const uint8_t *codes, int h, uint32
   }
 }
 
-// The power of two that brings a row whose largest magnitude has the fp32
-// exponent field e32 into [2^14, 2^15): 2^(141 - e32), at most 2^127 (rows of
-// zeros or of values below 2^-113).  Returns its exponent.
-__device__ __forceinline__ int row_scale_exp(uint32_t e32) {
-  return min(127, 141 - (int)e32);
-}
-
-// bf16 pairs -> the same values times s (a power of two) as f16 pairs (exact
-// but for the subnormal tail); 8 values per 16-byte vector.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float s) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(w[i] << 16) * s;
-    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * s;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(hi), "f"(lo));
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // Rows of x_perm (bf16 [rows, K]) -> f16 rows scaled by a power of two each
 // (see above); rscale[r] receives the inverse factor and hmax[r] is cleared
 // for the gate/up epilogue's maxima.  dst may equal src (each value is read
@@ -124,11 +98,7 @@ __global__ void __launch_bounds__(256) rows_f16_scaled_kernel(const __nv_bfloat1
   const int n4 = K / 8;
   uint32_t m = 0;  // largest |bf16| bit pattern of the lane's values (per half)
 #pragma unroll 8
-  for (int i = lane; i < n4; i += 32) {
-    const uint4 v = s4[i];
-    m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                             __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
-  }
+  for (int i = lane; i < n4; i += 32) m = bf16x8_absmax_bits(s4[i], m);
   m = max(m & 0xFFFFu, m >> 16);
   m = __reduce_max_sync(0xffffffffu, m);
   const int sx = row_scale_exp(m >> 7);  // bf16 and fp32 share the exponent field
@@ -155,7 +125,6 @@ __global__ void __launch_bounds__(128) h_rows_f16_scaled_kernel(
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int ok;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n4 = K / 8;
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     const int r0 = __ldg(offsets + e), r1 = __ldg(offsets + e + 1);
     if (r1 == r0) continue;
@@ -181,23 +150,8 @@ __global__ void __launch_bounds__(128) h_rows_f16_scaled_kernel(
     __syncthreads();
     if (!ok) return;
     for (int r = r0 + warp; r < r1; r += 4) {
-      const int sx = row_scale_exp(__ldcg(hmax + r) >> 23);
-      const float sc = ldexpf(1.0f, sx);
-      uint4 *row = reinterpret_cast<uint4 *>(h + (size_t)r * K);
-      for (int i0 = 0; i0 < n4; i0 += 32 * 8) {  // eight 16-byte loads in flight per lane
-        uint4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * 32 + lane;
-          if (i < n4) v[u] = __ldcg(row + i);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * 32 + lane;
-          if (i < n4) row[i] = bf16x8_to_f16x8_scaled(v[u], sc);
-        }
-      }
-      if (lane == 0) hscale[r] = ldexpf(1.0f, -sx);
+      const float inv = rescale_row_inplace(h + (size_t)r * K, K, __ldcg(hmax + r), lane);
+      if (lane == 0) hscale[r] = inv;
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncthreads();
@@ -512,10 +466,8 @@ moe_status launch_wt_bn(const moe_dims &d, const moe_experts &ex, const void *x_
   const long max_tt = Tk / BN + std::min<long>(d.E, Tk);
   const int sms = device_sm_count();
   __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(scr.h);
-  rows_f16_scaled_kernel<<<(unsigned)((Tk + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(x_perm), static_cast<__half *>(scr.x16), (int)Tk, d.H,
-      scr.xscale, scr.hmax);
-  if (cudaPeekAtLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_rows_f16_scaled(x_perm, scr.x16, Tk, d.H, scr.xscale, scr.hmax, stream) != MOE_OK)
+    return MOE_ERR_CUDA;
   // the tensor maps only move 2-byte elements: the bf16 maps serve the f16 rows
   {
     WtParams prm{};
@@ -607,6 +559,15 @@ moe_status launch_wt_fmt(const moe_dims &d, const moe_experts &ex, const void *x
 }
 
 }  // namespace
+
+moe_status launch_rows_f16_scaled(const void *x_perm, void *x16, long rows, int K, float *xscale,
+                                  uint32_t *hmax, cudaStream_t stream) {
+  if (rows == 0) return MOE_OK;
+  rows_f16_scaled_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(x_perm), static_cast<__half *>(x16), (int)rows, K, xscale,
+      hmax);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 // The K loops run in steps of four 64-wide slices per matrix pair (gate/up:
 // 2 slices of H, down: 4 slices of I).

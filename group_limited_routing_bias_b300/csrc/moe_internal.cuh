@@ -161,14 +161,17 @@ moe_status launch_route(const moe_dims &d, const void *x, const float *w_router,
                         float *logits = nullptr);
 
 // What the dispatch does with x after sorting: copy rows in bf16, copy them
-// as f16 (operands of the packed-weight GEMMs), or nothing (W4A4 quantises
-// while gathering, in launch_quantize_nvfp4).
-enum GatherMode { kGatherBf16 = 0, kGatherF16 = 1, kGatherNone = 2 };
+// as f16 scaled by a power of two per token (operands of the token-major
+// packed-weight GEMMs, rowscale.cuh; xscale and hmax as for
+// launch_rows_f16_scaled), or nothing (W4A4 quantises while gathering, in
+// launch_quantize_nvfp4).
+enum GatherMode { kGatherBf16 = 0, kGatherF16Scaled = 1, kGatherNone = 2 };
 
 moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
                           int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
                           int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream,
-                          GatherMode gather = kGatherBf16);
+                          GatherMode gather = kGatherBf16, float *xscale = nullptr,
+                          uint32_t *hmax = nullptr);
 
 // NVFP4 quantisation of bf16 rows.  With row_src, output row r (r < offsets[E],
 // read on the device) is x[row_src[r] / top_k]; otherwise row r is x[r], r < rows.
@@ -194,11 +197,6 @@ moe_status launch_experts(const moe_dims &d, const moe_experts &ex, const void *
                           const float *topk_w, void *y_partial, __nv_bfloat16 *h,
                           uint32_t *status, cudaStream_t stream);
 
-// NVFP4 or FP8 expert weights: x16 and h16 are f16 [Tk, H] and [Tk, I].
-moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const void *x16,
-                              const int32_t *expert_offsets, const int32_t *row_src,
-                              const float *topk_w, void *y_partial, void *h16, uint32_t *status,
-                              cudaStream_t stream);
 
 // NVFP4 or FP8 weights, small and mid-size batches: weights dequantised into
 // tensor memory, token rows on the MMA's N side, f16 operands with one
@@ -207,6 +205,12 @@ moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex, const vo
 // place); h [Tk, I] holds bf16 h, then its scaled f16 copy; xscale, hmax and
 // hscale are [Tk] scratch.  Used while the token tiles hold at most
 // kPackedWtMaxRows rows.
+// x_perm rows (bf16 [rows, K]) -> x16 (f16, may equal x_perm) scaled by a
+// power of two per row (rowscale.cuh); xscale[r] = the inverse factor, and
+// hmax[r] cleared for the gate/up epilogues' row maxima of h.
+moe_status launch_rows_f16_scaled(const void *x_perm, void *x16, long rows, int K, float *xscale,
+                                  uint32_t *hmax, cudaStream_t stream);
+
 struct PackedWtScratch {
   void *x16;
   void *h;
@@ -214,6 +218,14 @@ struct PackedWtScratch {
   uint32_t *hmax;
   float *hscale;
 };
+// NVFP4 or FP8 expert weights, the GEMMs with the dequantised weights in
+// shared memory (experts_packed.cu; token-major tiles from 64 rows up): scr
+// as above, with scr.x16 already holding the scaled f16 rows and xscale,
+// hmax set (launch_rows_f16_scaled or the scaled gather).
+moe_status launch_experts_fp4(const moe_dims &d, const moe_experts &ex,
+                              const int32_t *expert_offsets, const int32_t *row_src,
+                              const float *topk_w, void *y_partial, const PackedWtScratch &scr,
+                              uint32_t *status, cudaStream_t stream);
 constexpr int kPackedWtMaxRows = 64;
 bool packed_wt_applies(const moe_dims &d);
 moe_status launch_experts_packed_wt(const moe_dims &d, const moe_experts &ex, const void *x_perm,
@@ -232,7 +244,6 @@ moe_status launch_pack_nvfp4(int E, int N, int K, const uint8_t *q, const uint8_
 moe_status launch_pack_fp8(int E, int N, int K, const uint8_t *q, uint8_t *dst, cudaStream_t stream);
 
 // n bf16 values -> f16 (n even).
-moe_status launch_bf16_to_f16(const void *in, void *out, size_t n, cudaStream_t stream);
 
 moe_status launch_combine(const moe_dims &d, const void *y_partial, const int32_t *slot_of, void *y,
                           cudaStream_t stream);

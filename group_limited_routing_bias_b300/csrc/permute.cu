@@ -10,9 +10,12 @@
 //   permute_scatter_kernel one CTA per chunk: warp-ordered ranks -> slots
 //   permute_scatter_rows_kernel  all SMs: each token's x row to its k slots (16-byte
 //                          vectors, one warp per 2 KB segment of a row)
+//   permute_scatter_rows_scaled_kernel  the same as f16 scaled per token (one
+//                          warp per token), for the token-major packed GEMMs
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
+#include "rowscale.cuh"
 
 namespace beam {
 
@@ -201,15 +204,12 @@ __global__ void __launch_bounds__(kChunkThreads)
 // once and written to every permuted row that holds one of its entries
 // (slot_of[t*k + j]; dropped entries have slot -1).  Reading x once matters
 // when x is larger than L2 (prefill: an expert-ordered gather would fetch each
-// row from DRAM up to k times).  With TO_F16 the bf16 values are written as
-// f16 (exact for |v| >= 2^-14; the packed-weight GEMMs run on f16 operands).
-// One warp per (token, 128-vector segment of its row): each lane loads its
+// row from DRAM up to k times).  One warp per (token, 128-vector segment of its row): each lane loads its
 // four 16-byte vectors of the segment first, then stores them to the token's
 // k slots, so a warp has all its loads in flight at once and a small batch
 // still spreads over many warps.
 constexpr int kScatterSeg = 128;  // 16-byte vectors per warp task (4 per lane)
 
-template <bool TO_F16>
 __global__ void __launch_bounds__(256)
     permute_scatter_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
                                 int T, int top_k, int vec_per_row, uint4 *__restrict__ x_perm) {
@@ -227,15 +227,6 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < kScatterSeg / 32; ++i) {
       const int v = v0 + 32 * i;
       q[i] = v < vec_per_row ? src[v] : make_uint4(0u, 0u, 0u, 0u);
-      if (TO_F16) {
-        uint32_t *wd = reinterpret_cast<uint32_t *>(&q[i]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wd[c]));
-          const __half2 h = __float22half2_rn(f);
-          wd[c] = *reinterpret_cast<const uint32_t *>(&h);
-        }
-      }
     }
     for (int j = 0; j < top_k; ++j) {
       const int slot = __shfl_sync(0xffffffffu, my_slot, j);  // the same in every lane
@@ -248,12 +239,56 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same copy as f16 scaled by a power of two per token (rowscale.cuh):
+// one warp per token finds the row's largest magnitude, then converts and
+// writes the row to the token's slots; lane j records xscale and clears hmax
+// of slot j.  The second pass reads the row again, from L2.
+__global__ void __launch_bounds__(256)
+    permute_scatter_rows_scaled_kernel(const uint4 *__restrict__ x,
+                                       const int32_t *__restrict__ slot_of, int T, int top_k,
+                                       int vec_per_row, uint4 *__restrict__ x_perm, float *xscale,
+                                       uint32_t *hmax) {
+  const int lane = threadIdx.x & 31;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  for (long t = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    const int my_slot = lane < top_k ? __ldg(slot_of + (size_t)t * top_k + lane) : -1;
+    const uint4 *src = x + (size_t)t * vec_per_row;
+    uint32_t m = 0;
+#pragma unroll 8
+    for (int v = lane; v < vec_per_row; v += 32) m = bf16x8_absmax_bits(src[v], m);
+    m = max(m & 0xFFFFu, m >> 16);
+    m = __reduce_max_sync(0xffffffffu, m);
+    const int sx = row_scale_exp(m >> 7);
+    const float sc = ldexpf(1.0f, sx);
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 4) {
+      uint4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int v = v0 + 32 * i + lane;
+        q[i] = v < vec_per_row ? bf16x8_to_f16x8_scaled(src[v], sc) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, j);  // the same in every lane
+        if (slot < 0) continue;
+        uint4 *dst = x_perm + (size_t)slot * vec_per_row;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (v0 + 32 * i + lane < vec_per_row) dst[v0 + 32 * i + lane] = q[i];
+      }
+    }
+    if (my_slot >= 0) {
+      xscale[my_slot] = ldexpf(1.0f, -sx);
+      hmax[my_slot] = 0u;
+    }
+  }
+}
+
 }  // namespace
 
 moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void *x, void *x_perm,
                           int32_t *expert_offsets, int32_t *slot_of, int32_t *row_src,
                           int32_t *counts, int32_t *bases, uint32_t *status, cudaStream_t stream,
-                          GatherMode gather) {
+                          GatherMode gather, float *xscale, uint32_t *hmax) {
   const int Tk = d.T * d.top_k;
   const int nchunks = std::max(1, (Tk + kPermuteChunk - 1) / kPermuteChunk);
   const int scatter_smem = 32 * d.E * 4;  // at most 32 KB (E <= 256): no opt-in needed
@@ -268,17 +303,17 @@ moe_status launch_permute(const moe_dims &d, const int32_t *topk_idx, const void
     permute_scatter_kernel<<<nchunks, kChunkThreads, scatter_smem, stream>>>(
         topk_idx, Tk, d.E, bases, slot_of, row_src);
   }
-  if (Tk > 0 && gather != kGatherNone) {
+  if (Tk > 0 && gather == kGatherF16Scaled) {
+    const int blocks = (int)std::max<long>(1, std::min<long>(((long)d.T + 7) / 8, device_sm_count() * 8));
+    permute_scatter_rows_scaled_kernel<<<blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8, static_cast<uint4 *>(x_perm),
+        xscale, hmax);
+  } else if (Tk > 0 && gather == kGatherBf16) {
     const long tasks = (long)d.T * ((d.H / 8 + kScatterSeg - 1) / kScatterSeg);
     const int blocks = (int)std::max<long>(1, std::min<long>((tasks + 7) / 8, device_sm_count() * 8));
-    if (gather == kGatherF16)
-      permute_scatter_rows_kernel<true><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8,
-          static_cast<uint4 *>(x_perm));
-    else
-      permute_scatter_rows_kernel<false><<<blocks, 256, 0, stream>>>(
-          static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8,
-          static_cast<uint4 *>(x_perm));
+    permute_scatter_rows_kernel<<<blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(x), slot_of, d.T, d.top_k, d.H / 8,
+        static_cast<uint4 *>(x_perm));
   }
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

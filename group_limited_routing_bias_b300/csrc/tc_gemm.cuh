@@ -42,6 +42,8 @@
 //                                         SMs free up (griddepcontrol.launch_dependents)
 //   static constexpr bool PDL_SECONDARY;  launched as that dependent: the CTAs wait
 //                                         for the primary grid only before exiting
+//   static constexpr bool PDL_WAIT_B;     (CONVERT) the activation producer waits
+//                                         for the primary grid before its first load
 //   static bool tile_ready(const Params&, const Tile&, volatile int *abort)
 //                                         producer, before a tile's first load
 //                                         (false: gave up, the CTA aborts)
@@ -170,6 +172,17 @@ struct PdlSecondaryOf {
 template <class P>
 struct PdlSecondaryOf<P, std::void_t<decltype(P::PDL_SECONDARY)>> {
   static constexpr bool value = P::PDL_SECONDARY;
+};
+// Optional P::PDL_WAIT_B (with CONVERT): the activation tiles are the output
+// of the launch this one depends on; the activation producer alone waits for
+// it (griddepcontrol.wait) before its first load, the weights stream at once.
+template <class P, class = void>
+struct PdlWaitBOf {
+  static constexpr bool value = false;
+};
+template <class P>
+struct PdlWaitBOf<P, std::void_t<decltype(P::PDL_WAIT_B)>> {
+  static constexpr bool value = P::PDL_WAIT_B;
 };
 template <class P, class = void>
 struct HasTileReady : std::false_type {};
@@ -369,6 +382,9 @@ __global__ void __launch_bounds__(threads_for<P>(), 1)
       // (gated only by the converters freeing raw slots) and warp 3 issues the
       // activation tiles into the operand ring (gated by MMA completion).
       const bool raw_role = P::CONVERT && warp == 0;
+      if constexpr (P::CONVERT && PdlWaitBOf<P>::value) {
+        if (!raw_role) asm volatile("griddepcontrol.wait;" ::: "memory");
+      }
       int stage = 0, cur = blockIdx.x, tslot = 0;
       uint32_t ph = 0, issued = 0, par = 0, tph = 0;
       bool ok = true;

@@ -8,8 +8,8 @@ import torch
 
 import moe_inputs as mi
 import oracle
-from parity import (compare_routing, output_errors, reference_routing,
-                    sample_tokens)
+from parity import (compare_routing, output_errors, reference_routing, row_errors,
+                    sample_tokens, scale_rows)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -97,3 +97,30 @@ def test_fp8_tiled(lib, name, T, sample):
     y_rm = check(lib, case, sample)
     case.tiled = True
     assert torch.equal(forward(lib, case)[0], y_rm)
+
+
+@pytest.mark.parametrize("name,T", [("fp8", 64), ("tiny", 2), ("tiny", 2048)])
+def test_fp8_bf16_activation_range(lib, name, T):
+    """The three FP8 GEMM paths keep bf16's range (f16 operands scaled by a
+    power of two per token row): rows with |x| up to 1e5 and of about 1e-6,
+    each within the bf16 bars relative to its own scale.  fp8 T=64 runs the
+    tensor-memory GEMMs, tiny T=2 (I = 128) the weights-on-M ones with the
+    weights dequantised in shared memory, tiny T=2048 the token-major ones."""
+    case = Fp8Case(mi.CONFIGS[name], T=T)
+    n = 1 if T < 8 else 4
+    case.x_h = scale_rows(case.x_h, n=n)
+    case.x = case.x_h.to(DEV)
+    c = case.cfg
+    y, idx, w = forward(lib, case)
+    orc = oracle.route(mi.bf16_bits(case.x_h), case.wr_h.numpy(), case.b_h.numpy(), c.n_group,
+                       c.topk_group, c.top_k, c.routed_scale, details=True)
+    rep = compare_routing(orc, idx, w, c.n_group, c.topk_group, c.top_k, c.routed_scale)
+    assert rep.ok, (rep, rep.mismatch_info)
+    ridx, rw = reference_routing(orc, rep, idx, c.routed_scale)
+    tokens = np.arange(2 * n)
+    y_ref = oracle.experts_forward(mi.bf16_bits(case.x_h), ridx, rw, case.get_expert, tokens=tokens)
+    yg = y.double().cpu().numpy()[tokens]
+    assert np.isfinite(yg).all()
+    mx, fr = row_errors(yg, y_ref)
+    print(f"\n[{c.name} T={c.T}] rows |x|~1e5: rel-Frob {fr[:n]}; |x|~1e-6: {fr[n:]}")
+    assert (mx <= 2e-2).all() and (fr <= 5e-3).all(), (mx, fr)

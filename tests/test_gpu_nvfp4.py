@@ -104,11 +104,15 @@ def test_nvfp4_beam(lib, T, sample):
     check(lib, Fp4Case(mi.CONFIGS["nvfp4"], T=T), sample)
 
 
-def test_nvfp4_bf16_activation_range(lib):
-    """The packed-weight path of decode-sized batches (weights dequantised into
-    tensor memory, bf16 activations): token rows with |x| up to 1e5 and rows
-    of about 1e-6, every row within the bf16 bars relative to its own scale."""
-    case = Fp4Case(mi.CONFIGS["nvfp4"], T=64)
+@pytest.mark.parametrize("name,T", [("nvfp4", 64), ("tiny-nvfp4", 2048)])
+def test_nvfp4_bf16_activation_range(lib, name, T):
+    """Both packed-weight paths keep bf16's range (f16 operands scaled by a
+    power of two per token row): token rows with |x| up to 1e5 (h ~ 1e10) and
+    rows of about 1e-6, every row within the bf16 bars relative to its own
+    scale.  The NVFP4 workload at T=64 runs the GEMMs with the weights
+    dequantised into tensor memory, the tiny shape at T=2048 the token-major
+    ones."""
+    case = Fp4Case(mi.CONFIGS["nvfp4"] if name == "nvfp4" else TINY4, T=T)
     case.x_h = scale_rows(case.x_h)
     case.x = case.x_h.to(DEV)
     c = case.cfg
@@ -123,7 +127,7 @@ def test_nvfp4_bf16_activation_range(lib):
     yg = y.double().cpu().numpy()[tokens]
     assert np.isfinite(yg).all()
     mx, fr = row_errors(yg, y_ref)
-    print(f"\n[nvfp4 T=64] rows |x|~1e5: rel-Frob {fr[:4]}; |x|~1e-6: {fr[4:8]}")
+    print(f"\n[{c.name} T={c.T}] rows |x|~1e5: rel-Frob {fr[:4]}; |x|~1e-6: {fr[4:8]}")
     assert (mx <= 2e-2).all() and (fr <= 5e-3).all(), (mx, fr)
 
 
