@@ -212,7 +212,13 @@ moe_status moe_permute(const moe_dims *dims, const int32_t *topk_idx, const void
  *   h = silu(x_perm . W_gate[e]^T) * (x_perm . W_up[e]^T)     (h kept in bf16)
  *   y_partial[r] = topk_w[row_src[r]] * (h . W_down[e]^T)      (stored bf16)
  * for every permuted row r of expert e.  fp32 accumulation on tensor cores.
- * topk_w is indexed by entry (t*k + j).  Workspace: MOE_OP_EXPERTS.
+ * With NVFP4 or FP8 weights (MOE_W_NVFP4, MOE_W_FP8) the GEMMs run on f16
+ * operands: the dequantised weights are exact in f16, and x_perm and h keep
+ * bf16's range by one power-of-two scale per row (each row's largest
+ * magnitude brought into [2^14, 2^15), multiplied back out of the fp32
+ * accumulator), so the results are those of bf16 activations up to values
+ * below 2^-28 of their row's largest.  topk_w is indexed by entry (t*k + j).
+ * Workspace: MOE_OP_EXPERTS.
  */
 moe_status moe_experts_swiglu(const moe_dims *dims, const moe_experts *experts,
                               const void *x_perm, const int32_t *expert_offsets,
