@@ -65,11 +65,12 @@ __device__ __forceinline__ void nvfp4_half_f16(uint4 c, uint32_t scales, int h,
   }
 }
 
-// Half h of one FP8 weight row of a 64-wide K slice: 32 e4m3 codes -> 16 f16 pairs.
-__device__ __forceinline__ void fp8_half_f16(const uint8_t *codes, int h, uint32_t (&out)[16]) {
+// Half of one FP8 weight row of a 64-wide K slice: 32 e4m3 codes (two 16-byte
+// vectors) -> 16 f16 pairs.
+__device__ __forceinline__ void fp8_half_f16(const uint4 *codes, uint32_t (&out)[16]) {
 #pragma unroll
   for (int v = 0; v < 2; ++v) {
-    const uint4 q = *reinterpret_cast<const uint4 *>(codes + 32 * h + 16 * v);
+    const uint4 q = codes[v];
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -163,33 +164,46 @@ __global__ void __launch_bounds__(128) h_rows_f16_scaled_kernel(
 }
 
 // Raw layouts of one 128-row A tile of a K slice in a ring slot, per format.
+// A converter thread first loads all its row's packed bytes into registers
+// (load), then converts the row in two halves of 32 k (convert).
+struct WtRow {
+  uint4 q[4];   // NVFP4: q[0..1] = 32 code bytes; FP8: 64 code bytes
+  uint32_t sc;  // NVFP4: the four e4m3 block scales of the slice
+};
 // Row-major NVFP4 arrives as TMA boxes: codes [128][32 B], then scale boxes
 // [128][16 B] (the 16 scales of 256 k; this slice's four at (k % 4) * 4).
 struct WtNvfp4 {
   static constexpr bool kTiled = false, kPerRowScale = false;
   static constexpr int kTileBytes = 128 * 48;
-  __device__ static void convert(const uint8_t *t, int k, int r, int h, uint32_t (&out)[16]) {
-    const uint4 c = reinterpret_cast<const uint4 *>(t + r * 32)[h];
-    const uint32_t sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 16 + (k & 3) * 4);
-    nvfp4_half_f16(c, sc, h, out);
+  __device__ static void load(const uint8_t *t, int k, int r, WtRow &w) {
+    w.q[0] = reinterpret_cast<const uint4 *>(t + r * 32)[0];
+    w.q[1] = reinterpret_cast<const uint4 *>(t + r * 32)[1];
+    w.sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 16 + (k & 3) * 4);
+  }
+  __device__ static void convert(const WtRow &w, int h, uint32_t (&out)[16]) {
+    nvfp4_half_f16(w.q[h], w.sc, h, out);
   }
 };
 // Tiled NVFP4 (moe_pack_nvfp4): codes [128][32 B], then scales [128][4 B].
-struct WtNvfp4Tiled {
-  static constexpr bool kTiled = true, kPerRowScale = false;
+struct WtNvfp4Tiled : WtNvfp4 {
+  static constexpr bool kTiled = true;
   static constexpr int kTileBytes = 4608;
-  __device__ static void convert(const uint8_t *t, int, int r, int h, uint32_t (&out)[16]) {
-    const uint4 c = reinterpret_cast<const uint4 *>(t + r * 32)[h];
-    const uint32_t sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 4);
-    nvfp4_half_f16(c, sc, h, out);
+  __device__ static void load(const uint8_t *t, int, int r, WtRow &w) {
+    w.q[0] = reinterpret_cast<const uint4 *>(t + r * 32)[0];
+    w.q[1] = reinterpret_cast<const uint4 *>(t + r * 32)[1];
+    w.sc = *reinterpret_cast<const uint32_t *>(t + 128 * 32 + r * 4);
   }
 };
 // FP8, row-major (TMA box) or tiled (moe_pack_fp8): codes [128][64 B].
 struct WtFp8 {
   static constexpr bool kTiled = false, kPerRowScale = true;
   static constexpr int kTileBytes = 8192;
-  __device__ static void convert(const uint8_t *t, int, int r, int h, uint32_t (&out)[16]) {
-    fp8_half_f16(t + r * 64, h, out);
+  __device__ static void load(const uint8_t *t, int, int r, WtRow &w) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) w.q[v] = reinterpret_cast<const uint4 *>(t + r * 64)[v];
+  }
+  __device__ static void convert(const WtRow &w, int h, uint32_t (&out)[16]) {
+    fp8_half_f16(&w.q[2 * h], out);
   }
 };
 struct WtFp8Tiled : WtFp8 {
@@ -305,9 +319,13 @@ struct ExpertGemmWT {
       }
     }
   }
-  __device__ static void convert_row(const Params &, const Tile &, int s, const uint8_t *raw,
-                                     int j, int a, int row, int h, uint32_t (&out)[16]) {
-    Fmt::convert(raw + (j * NA + a) * Fmt::kTileBytes, s * KS + j, row, h, out);
+  using Row = WtRow;
+  __device__ static void load_row(const Params &, const Tile &, int s, const uint8_t *raw, int j,
+                                  int a, int row, Row &w) {
+    Fmt::load(raw + (j * NA + a) * Fmt::kTileBytes, s * KS + j, row, w);
+  }
+  __device__ static void convert_half(const Row &w, int h, uint32_t (&out)[16]) {
+    Fmt::convert(w, h, out);
   }
   // gate/up: each epilogue warp counts its 32 features of h for the tile (its
   // stores and row maxima before the count); the h rescaling kernel waits for

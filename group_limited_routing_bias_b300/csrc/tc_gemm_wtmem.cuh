@@ -53,10 +53,11 @@
 //   static void load_b(const Params&, const Tile&, int s, uint8_t *bslot, uint64_t *bar)
 //                                       (KS tiles of BN rows x 128 bytes)
 //   static void load_raw(const Params&, const Tile&, int s, uint8_t *raw, uint64_t *bar)
-//   static void convert_row(const Params&, const Tile&, int s, const uint8_t *raw, int j,
-//                           int a, int row, int h, uint32_t (&out)[16])
-//                                       (slice j of the step, matrix a, half h: f16
-//                                        pairs of k 32h .. 32h + 31)
+//   struct Row;                         (one weight row's packed bytes in registers)
+//   static void load_row(const Params&, const Tile&, int s, const uint8_t *raw, int j,
+//                        int a, int row, Row&)   (slice j of the step, matrix a)
+//   static void convert_half(const Row&, int h, uint32_t (&out)[16])
+//                                       (f16 pairs of k 32h .. 32h + 31)
 //   static void epilogue(const Params&, const Tile&, uint32_t taddr, int row)
 //   optional tile_ready / tile_done / last_cta hooks as in tc_gemm.cuh.
 #pragma once
@@ -384,15 +385,21 @@ __global__ void __launch_bounds__(kWtThreads, 1)
           break;
         }
         tc_fence_after();
-        // two halves of 32 k: the first half's store runs while the second
-        // half converts
+        // the row's packed bytes into registers, then two halves of 32 k, the
+        // first half's store running while the second half converts.  The
+        // ring slot goes back to the producer only once the converted values
+        // exist: an mbarrier arrival does not wait for the thread's
+        // shared-memory loads still in flight (releasing the slot right after
+        // the loads let the next TMA copy overwrite bytes not yet read)
+        typename P::Row w;
+        P::load_row(p, tile, s, raws + rs * P::RAW_BYTES, j, a, row, w);
         uint32_t v[16];
-        P::convert_row(p, tile, s, raws + rs * P::RAW_BYTES, j, a, row, 0, v);
+        P::convert_half(w, 0, v);
         tmem_st16(tq + as * kStageCols, v);
-        P::convert_row(p, tile, s, raws + rs * P::RAW_BYTES, j, a, row, 1, v);
+        P::convert_half(w, 1, v);
         tmem_st16(tq + as * kStageCols + 16, v);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rs]);  // the packed bytes are in registers
+        if (lane == 0) mbar_arrive(&raw_empty[rs]);
         tmem_wait_st();
         // the stage is complete for the MMA once its B tiles have landed too:
         // one warp checks (the stage completes only with every warp's arrival,
