@@ -348,15 +348,14 @@ moe_status moe_forward(const moe_dims *dims, const void *x, const float *w_route
                               at<uint32_t>(ws, L.hmax), at<float>(ws, L.hscale)};
     st = launch_experts_packed_wt(d, *experts, x_perm, offsets, row_src, w, y_partial, scr, status,
                                   s);
-  }
-  else if (fp4) {
+  } else if (fp4) {
     const PackedWtScratch scr{x_perm, at<void>(ws, L.h), at<float>(ws, L.xscale),
                               at<uint32_t>(ws, L.hmax), at<float>(ws, L.hscale)};
     st = launch_experts_fp4(d, *experts, offsets, row_src, w, y_partial, scr, status, s);
-  }
-  else
+  } else {
     st = launch_experts(d, *experts, x_perm, offsets, row_src, w, y_partial,
                         at<__nv_bfloat16>(ws, L.h), status, s);
+  }
   if (st != MOE_OK) return st;
   return launch_combine(d, y_partial, slot_of, y, s);
 }
