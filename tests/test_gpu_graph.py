@@ -17,19 +17,27 @@ def lib():
     return m
 
 
-@pytest.mark.parametrize("T,weights", [(64, "bf16"), (2048, "bf16"), (200, "nvfp4-a4")])
+@pytest.mark.parametrize("T,weights", [(64, "bf16"), (2048, "bf16"), (200, "nvfp4-a4"),
+                                       (64, "nvfp4"), (2048, "nvfp4"), (64, "fp8"), (2048, "fp8")])
 def test_graph_replay_matches_eager(lib, T, weights):
+    """The packed W4A16 / W8A16 cases cover both packed GEMM paths (T=64: the
+    tensor-memory GEMMs and their chain of four dependent launches; T=2048:
+    the token-major ones with the scaled gather and the h rescaling)."""
     cfg = mi.CONFIGS["tiny"].with_T(T)
-    if weights == "nvfp4-a4":
-        cfg = mi.MoeConfig("tiny-nvfp4", T=T, H=256, E=32, n_group=8, topk_group=2, top_k=4, I=256,
+    if weights != "bf16":
+        cfg = mi.MoeConfig("tiny-packed", T=T, H=256, E=32, n_group=8, topk_group=2, top_k=4, I=256,
                            weights="nvfp4")
     x, wr, b = (t.to(DEV) for t in mi.make_router_inputs(cfg, seed=3))
     w = mi.make_expert_weights(cfg, device=DEV, seed=3)
     if weights == "bf16":
         ex = lib.Experts(*w)
+    elif weights == "fp8":
+        packed = [mi.quantize_experts_fp8(t) for t in w]
+        ex = lib.Experts(*[p[0] for p in packed], None, None, None, *[p[1] for p in packed])
     else:
         packed = [mi.quantize_experts_nvfp4(t) for t in w]
-        ex = lib.Experts(*[p[i] for i in range(3) for p in packed], a4=(mi.A4_X_GLOBAL, mi.A4_H_GLOBAL))
+        a4 = (mi.A4_X_GLOBAL, mi.A4_H_GLOBAL) if weights == "nvfp4-a4" else None
+        ex = lib.Experts(*[p[i] for i in range(3) for p in packed], a4=a4)
     d = lib.dims_of(cfg)
     ws = lib.alloc_workspace(d, lib.MOE_OP_FORWARD, ex.dtype)
     y = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=DEV)
