@@ -610,7 +610,8 @@ def main():
         torch.cuda.empty_cache()
         packed = [mi.quantize_experts_fp8(w) for w in weights]
         fp8w = tuple(p[0] for p in packed) + (None, None, None) + tuple(p[1] for p in packed)
-        fp8 = packed_figures(lib, mi, "fp8", fp8w, FP8_EXPERT_BYTES, dev, flush, peaks, tiled=True)
+        fp8 = packed_figures(lib, mi, "fp8", fp8w, FP8_EXPERT_BYTES, dev, flush, peaks, tiled=True,
+                             extra_T=(1, 1024))
         del packed, fp8w
         torch.cuda.empty_cache()
 
