@@ -242,7 +242,10 @@ template <class Fmt, int BN_, bool GATEUP>
 struct ExpertGemmWT {
   static constexpr int BN = BN_;
   static constexpr int NA = GATEUP ? 2 : 1;
-  static constexpr int NBUF = 2 * NA * BN <= 256 ? 2 : 1;  // leave columns for the A stages
+  // two accumulator sets only while three A stages still fit beside them: the
+  // converters are the bound, and with two stages they wait for the MMA to
+  // free one every step
+  static constexpr int NBUF = 512 - 2 * NA * BN >= 3 * kWtTilesPerStep * 32 ? 2 : 1;
   static constexpr int KS = kWtTilesPerStep / NA;           // 64-wide K slices per step
   // stages of four A tiles: what tensor memory holds beside the accumulators (at most 4)
   static constexpr int AST_FIT = (512 - NBUF * NA * BN) / (kWtTilesPerStep * 32);
