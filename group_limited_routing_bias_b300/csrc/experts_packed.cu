@@ -406,8 +406,9 @@ struct ExpertGemmTMFP4 {
   __device__ static void epilogue(const Params &p, const Tile &t, uint32_t taddr, int row) {
     const bool valid = row < t.nrows;
     const int n0 = t.f * FW;  // first output feature of the tile
-    // this thread's token row: its inverse activation factor (rowscale.cuh)
-    const float bs = valid ? __ldg(p.bscale + t.row0 + row) : 0.f;
+    // this thread's token row: its inverse activation factor (rowscale.cuh;
+    // for down written by the kernel this launch depends on: read from L2)
+    const float bs = valid ? __ldcg(p.bscale + t.row0 + row) : 0.f;
     if (GATEUP) {
       __nv_bfloat16 *dst =
           static_cast<__nv_bfloat16 *>(p.out) + (size_t)(t.row0 + row) * p.out_cols + n0;
