@@ -70,6 +70,13 @@ def test_workspace_sizes(lib):
     assert sizes[lib.MOE_OP_EXPERTS] >= Tk * 2560 * 2
     assert sizes[lib.MOE_OP_FORWARD] > max(sizes[o] for o in range(3))
     assert lib.workspace_size(lib.make_dims(64, 5000, 256, 8, 4, 8, 2560, 2.5), 3) == 0
+    # packed weights add the per-row factors of x and h and the row maxima of
+    # h ([Tk] fp32 each); the staged experts call also an f16 copy of x_perm
+    for wd in (lib.MOE_W_NVFP4, lib.MOE_W_FP8):
+        fwd = lib.workspace_size(d, lib.MOE_OP_FORWARD, wd)
+        exp = lib.workspace_size(d, lib.MOE_OP_EXPERTS, wd)
+        assert fwd >= sizes[lib.MOE_OP_FORWARD] + 3 * Tk * 4
+        assert exp >= sizes[lib.MOE_OP_EXPERTS] + Tk * 5120 * 2 + 3 * Tk * 4
 
 
 def test_argument_errors_return_before_launch(lib):
