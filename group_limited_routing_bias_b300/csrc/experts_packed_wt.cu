@@ -256,9 +256,11 @@ struct ExpertGemmWT {
   static constexpr int B_SLOT = KS * BN * kTileK * 2;
   static constexpr int BS_FIT = (kSmemLimit / 2) / B_SLOT;
   static constexpr int BS = BS_FIT > 6 ? 6 : BS_FIT < 2 ? 2 : BS_FIT;
-  // raw ring: what shared memory holds beside the activation slots (at most 8 steps)
+  // raw ring: what shared memory holds beside the activation slots (at most 8
+  // steps), leaving 2 KB of the SM free so that a CTA of the h rescaling
+  // kernel fits beside this one
   static constexpr int RS_FIT =
-      (kSmemLimit - 2048 - (int)sizeof(TileSched) - BS * KS * BN * kTileK * 2) / RAW_BYTES;
+      (kSmemLimit - 2048 - (int)sizeof(TileSched) - BS * KS * BN * kTileK * 2 - 2048) / RAW_BYTES;
   static constexpr int RS = RS_FIT > 8 ? 8 : RS_FIT;
   static_assert(AST >= 2 && RS >= 2, "pipeline depth");
   static constexpr bool DYNAMIC = true;
